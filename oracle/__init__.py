@@ -1,0 +1,6 @@
+"""Float64 CPU oracle (test infrastructure only; see ``oracle.ref``)."""
+from .ref import (attn_bwd, attn_fwd, attn_rows, brute_force_masked, default_scale,
+                  pack_plan, rope, rope_angles)
+
+__all__ = ["pack_plan", "rope", "rope_angles", "attn_fwd", "attn_bwd", "attn_rows",
+           "brute_force_masked", "default_scale"]

@@ -1,0 +1,284 @@
+"""Float64 CPU oracle for packed native-resolution joint attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import or run this module.  The CUDA
+library never calls it and shares no code, table or helper with it.
+
+What it computes, and where each step comes from:
+
+* ``pack_plan`` -- Mage-Flow review (startedourmission.github.io),
+  section "Native-Resolution MMDiT": images of different sizes are encoded to
+  variable-length latent token rows and packed back to back into one batch
+  under a fixed token budget; text is packed the same way, unpadded; attention
+  is confined to each sample by per-sample cumulative offsets instead of a
+  block-diagonal mask.  Section "Mage-VAE": the latent is 16x downsampled with
+  patchification absorbed, so an H x W image gives (H/16)(W/16) tokens.
+* ``rope`` -- per-sample 2D rotary embedding (Hugging Face paper page,
+  Highlights, "System-level speed"; model card, section "Architecture").  The
+  pages do not give the layout; this library fixes it: head_dim split in half,
+  first half rotated by the token's latent row, second half by its column,
+  pair (2i, 2i+1) of each half at frequency theta^(-2i/(head_dim/2)),
+  theta = 10000, rotation x0' = x0 cos - x1 sin, x1' = x0 sin + x1 cos; text
+  tokens are not rotated.
+* ``attn_fwd`` / ``attn_bwd`` -- joint text+image self-attention of each
+  sample (review, "Native-Resolution MMDiT": text and image tokens are
+  concatenated and processed by joint self-attention), i.e. plain
+  softmax(s * q~ k~^T) v per sample and head, with s = 1/sqrt(head_dim) unless
+  given; the backward is the exact gradient of that definition with respect
+  to the un-rotated q, k and v.
+* ``brute_force_masked`` -- the thing the offsets replace: dense attention
+  over the whole pack with an explicit block-diagonal mask.  Written
+  separately from ``attn_fwd`` on purpose.
+
+Every array is float64; bf16 inputs are widened exactly.  Nothing is blocked,
+fused or reordered beyond the definitions above.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+PATCH = 16
+TEXT_POS = -1
+
+
+# --------------------------------------------------------------------------
+# Pack plan
+# --------------------------------------------------------------------------
+
+def pack_plan(samples, token_budget: int = 0):
+    """Plan a pack from per-sample (text_len, height_px, width_px).
+
+    The samples are taken in order; the pack is the longest prefix whose total
+    token count stays within ``token_budget`` (0 = no budget).  Tokens of one
+    sample are [text; image], the image in row-major latent order (row = index
+    along the height).  Returns a dict with ``n_samples`` (packed prefix),
+    ``cu_seqlens`` int32 [n+1], ``pos`` int32 [T, 2] ((-1, -1) for text),
+    ``total_tokens``, ``max_seqlen`` and ``max_grid`` (largest grid side).
+    Raises ValueError for invalid shapes and when not even the first sample
+    fits the budget.
+    """
+    lens, grids = [], []
+    for (t, h, w) in samples:
+        if t < 0 or h <= 0 or w <= 0 or h % PATCH or w % PATCH:
+            raise ValueError(f"invalid sample {(t, h, w)}")
+        gh, gw = h // PATCH, w // PATCH
+        lens.append(t + gh * gw)
+        grids.append((gh, gw))
+    n = 0
+    used = 0
+    for L in lens:
+        if token_budget > 0 and used + L > token_budget:
+            break
+        used += L
+        n += 1
+    if n == 0 and len(samples) > 0:
+        raise ValueError("first sample exceeds the token budget")
+    cu = np.zeros(n + 1, dtype=np.int32)
+    for i in range(n):
+        cu[i + 1] = cu[i] + lens[i]
+    T = int(cu[n])
+    pos = np.full((T, 2), TEXT_POS, dtype=np.int32)
+    for i in range(n):
+        t = samples[i][0]
+        gh, gw = grids[i]
+        for j in range(gh * gw):
+            pos[cu[i] + t + j, 0] = j // gw
+            pos[cu[i] + t + j, 1] = j % gw
+    return {
+        "n_samples": n,
+        "cu_seqlens": cu,
+        "pos": pos,
+        "total_tokens": T,
+        "max_seqlen": int(max(lens[:n])) if n else 0,
+        "max_grid": int(max(max(g) for g in grids[:n])) if n else 0,
+    }
+
+
+# --------------------------------------------------------------------------
+# 2D RoPE
+# --------------------------------------------------------------------------
+
+def rope_angles(pos, head_dim: int, theta: float = 10000.0):
+    """Angle of every rotation pair: [T, head_dim/2] float64.
+
+    Pair index p < head_dim/4 lives in the first half and turns by
+    row * f_p; pair index head_dim/4 + p lives in the second half and turns by
+    col * f_p, with f_p = theta^(-2p/(head_dim/2)).  Text rows get angle 0.
+    """
+    half = head_dim // 2
+    nfreq = half // 2
+    f = np.array([theta ** (-2.0 * p / half) for p in range(nfreq)], dtype=np.float64)
+    pos = np.asarray(pos)
+    row = pos[:, 0].astype(np.float64)
+    col = pos[:, 1].astype(np.float64)
+    ang = np.concatenate([row[:, None] * f[None, :], col[:, None] * f[None, :]], axis=1)
+    ang[pos[:, 0] < 0] = 0.0
+    return ang
+
+
+def rope(x, pos, theta: float = 10000.0, inverse: bool = False):
+    """Rotate x [T, heads, head_dim] by each token's 2D position.
+
+    Pair m covers dims (2m, 2m+1) over the whole head (m < head_dim/2), which
+    puts the first head_dim/4 pairs in the first half and the rest in the
+    second half.  ``inverse`` rotates by the negated angles (R^T), which is
+    the adjoint needed to pull gradients back to un-rotated inputs.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T, H, D = x.shape
+    ang = rope_angles(pos, D, theta)
+    if inverse:
+        ang = -ang
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    x0 = x[..., 0::2]
+    x1 = x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x0 * c - x1 * s
+    out[..., 1::2] = x0 * s + x1 * c
+    return out
+
+
+# --------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)
+
+
+def _logsumexp_rows(S):
+    m = S.max(axis=1, keepdims=True)
+    return (m + np.log(np.exp(S - m).sum(axis=1, keepdims=True)))[:, 0]
+
+
+def attn_fwd(q, k, v, cu_seqlens, pos, softmax_scale: float = 0.0, theta: float = 10000.0):
+    """Per-sample, per-head softmax attention on RoPE-rotated q and k.
+
+    q, k, v: [T, H, D] (any float dtype, widened to float64).
+    Returns O [T, H, D] float64 and LSE [H, T] float64, where LSE is the
+    natural log-sum-exp of the scaled logits of each query row.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    T, H, D = q.shape
+    s = softmax_scale if softmax_scale > 0 else default_scale(D)
+    qr = rope(q, pos, theta)
+    kr = rope(k, pos, theta)
+    O = np.zeros((T, H, D))
+    LSE = np.zeros((H, T))
+    for i in range(len(cu_seqlens) - 1):
+        a, b = int(cu_seqlens[i]), int(cu_seqlens[i + 1])
+        for h in range(H):
+            S = s * (qr[a:b, h, :] @ kr[a:b, h, :].T)
+            lse = _logsumexp_rows(S)
+            P = np.exp(S - lse[:, None])
+            O[a:b, h, :] = P @ v[a:b, h, :]
+            LSE[h, a:b] = lse
+    return O, LSE
+
+
+def attn_bwd(q, k, v, o, lse, do, cu_seqlens, pos, softmax_scale: float = 0.0,
+             theta: float = 10000.0):
+    """Gradients dQ, dK, dV of sum(O * dO) w.r.t. the un-rotated q, k, v.
+
+    With q~ = R q, k~ = R k, S = s q~ k~^T, P = exp(S - LSE):
+      dV = P^T dO;  dP = dO V^T;  D = rowsum(dO * O);  dS = P * (dP - D);
+      dq~ = s dS k~;  dk~ = s dS^T q~;  dq = R^T dq~;  dk = R^T dk~.
+    ``o`` and ``lse`` are the forward's outputs (as the backward of the
+    library receives them).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    o = np.asarray(o, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    T, H, D = q.shape
+    s = softmax_scale if softmax_scale > 0 else default_scale(D)
+    qr = rope(q, pos, theta)
+    kr = rope(k, pos, theta)
+    dqr = np.zeros((T, H, D))
+    dkr = np.zeros((T, H, D))
+    dv = np.zeros((T, H, D))
+    for i in range(len(cu_seqlens) - 1):
+        a, b = int(cu_seqlens[i]), int(cu_seqlens[i + 1])
+        for h in range(H):
+            S = s * (qr[a:b, h, :] @ kr[a:b, h, :].T)
+            P = np.exp(S - lse[h, a:b][:, None])
+            dv[a:b, h, :] = P.T @ do[a:b, h, :]
+            dP = do[a:b, h, :] @ v[a:b, h, :].T
+            Drow = (do[a:b, h, :] * o[a:b, h, :]).sum(axis=1)
+            dS = P * (dP - Drow[:, None])
+            dqr[a:b, h, :] = s * (dS @ kr[a:b, h, :])
+            dkr[a:b, h, :] = s * (dS.T @ qr[a:b, h, :])
+    dq = rope(dqr, pos, theta, inverse=True)
+    dk = rope(dkr, pos, theta, inverse=True)
+    return dq, dk, dv
+
+
+def attn_rows(q, k, v, cu_seqlens, pos, rows, head: int, softmax_scale: float = 0.0,
+              theta: float = 10000.0):
+    """O and LSE of selected query rows of one head, one row at a time.
+
+    For full-size packs: each row touches only its own sample's keys, so it
+    costs O(L * D).  Returns (O [len(rows), D], LSE [len(rows)]).
+    """
+    q = np.asarray(q[:, head, :], dtype=np.float64)[:, None, :]
+    k = np.asarray(k[:, head, :], dtype=np.float64)[:, None, :]
+    v = np.asarray(v[:, head, :], dtype=np.float64)
+    D = q.shape[2]
+    s = softmax_scale if softmax_scale > 0 else default_scale(D)
+    cu = np.asarray(cu_seqlens)
+    O = np.zeros((len(rows), D))
+    LSE = np.zeros(len(rows))
+    for n, r in enumerate(rows):
+        i = int(np.searchsorted(cu, r, side="right") - 1)
+        a, b = int(cu[i]), int(cu[i + 1])
+        qr = rope(q[r:r + 1], pos[r:r + 1], theta)[0, 0]
+        kr = rope(k[a:b], pos[a:b], theta)[:, 0, :]
+        srow = s * (kr @ qr)
+        m = srow.max()
+        lse = m + math.log(np.exp(srow - m).sum())
+        O[n] = np.exp(srow - lse) @ v[a:b]
+        LSE[n] = lse
+    return O, LSE
+
+
+def brute_force_masked(q, k, v, cu_seqlens, pos, softmax_scale: float = 0.0,
+                       theta: float = 10000.0):
+    """Dense attention over all T tokens with an explicit block-diagonal mask.
+
+    Independent of ``attn_fwd``: the rotation is applied through complex
+    multiplication of (x_{2m} + i x_{2m+1}) by exp(i * angle), the mask is a
+    T x T boolean matrix built from a per-token sample id, and the softmax is
+    taken over the full masked row.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    T, H, D = q.shape
+    s = softmax_scale if softmax_scale > 0 else default_scale(D)
+    ang = rope_angles(pos, D, theta)                     # [T, D/2]
+    rot = np.exp(1j * ang)[:, None, :]
+    qc = (q[..., 0::2] + 1j * q[..., 1::2]) * rot
+    kc = (k[..., 0::2] + 1j * k[..., 1::2]) * rot
+    sid = np.zeros(T, dtype=np.int64)
+    for i in range(len(cu_seqlens) - 1):
+        sid[int(cu_seqlens[i]):int(cu_seqlens[i + 1])] = i
+    allowed = sid[:, None] == sid[None, :]
+    O = np.zeros((T, H, D))
+    LSE = np.zeros((H, T))
+    for h in range(H):
+        # Re(a * conj(b)) = a0 b0 + a1 b1 is the real dot product of the pairs.
+        S = s * np.real(qc[:, h, :] @ np.conj(kc[:, h, :]).T)
+        S = np.where(allowed, S, -np.inf)
+        m = S.max(axis=1, keepdims=True)
+        E = np.where(allowed, np.exp(S - m), 0.0)
+        Z = E.sum(axis=1, keepdims=True)
+        O[:, h, :] = (E / Z) @ v[:, h, :]
+        LSE[h] = (m + np.log(Z))[:, 0]
+    return O, LSE
