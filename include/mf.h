@@ -1,0 +1,179 @@
+/*
+ * mf.h -- packed native-resolution joint attention for NVIDIA B300 (sm_103a).
+ *
+ * The operation (Mage-Flow, "An Efficient Native-Resolution Foundation Model
+ * for Image Generation and Editing"; review page, section "Native-Resolution
+ * MMDiT"; Hugging Face paper page, Highlights "Native resolution" and
+ * "System-level speed"; model card, section "Architecture"):
+ *
+ *   Images of different sizes become 16x-downsampled latent grids of
+ *   (H/16)*(W/16) tokens (review, section "Mage-VAE": patchification is
+ *   absorbed into the tokenizer).  Each sample's text tokens and image tokens
+ *   are concatenated [text; image] and samples are packed back to back under a
+ *   token budget.  Joint self-attention runs inside each sample only, confined
+ *   by cumulative per-sample offsets (cu_seqlens) instead of a mask, with
+ *   per-sample 2D rotary embedding on Q and K.
+ *
+ * RoPE layout (the pages name per-sample 2D RoPE but not its layout; this
+ * library fixes it): head_dim split in half, the first half rotated by the
+ * token's latent row, the second half by its column; pair (2i, 2i+1) of a half
+ * turns at frequency theta^(-2i/(head_dim/2)); x0' = x0 cos - x1 sin,
+ * x1' = x0 sin + x1 cos; text tokens are not rotated.  Image token j of a
+ * sample (0-based, row-major, row = index along the height) has
+ * (row, col) = (j / (W/16), j % (W/16)).
+ *
+ * Conventions shared by every call:
+ *   - Device tensors are caller-owned and contiguous.  Q, K, V, O, dO, dQ, dK,
+ *     dV are bf16 [total_tokens, heads, head_dim] (row stride heads*head_dim),
+ *     16-byte aligned.  LSE is float32 [heads, total_tokens], natural log of
+ *     the scaled logits' sum of exponentials.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     launch is enqueued on it.  Only mf_pack_plan and mf_check synchronize
+ *     it (to return scalars); the attention calls never do.
+ *   - The library allocates no device memory: the caller passes workspaces
+ *     sized by the *_workspace_size calls.  It keeps no state besides a
+ *     per-thread copy of the last CUDA error message.
+ *   - Arguments are validated before anything is launched; a bad argument
+ *     returns MF_ERR_INVALID_ARG and leaves every buffer untouched.
+ *   - Every wait inside a kernel is bounded (a few seconds).  A kernel that
+ *     gives up sets the plan's device status word and exits cleanly;
+ *     mf_check() reports it as MF_ERR_TIMEOUT.
+ *   - softmax_scale <= 0 selects 1/sqrt(head_dim).
+ *   - Precision: Q, K, V, O and the gradients are bf16 with fp32
+ *     accumulation.  The logit product R(Q) R(K)^T is computed from fp16
+ *     copies of the rotated rows (R(Q) pre-multiplied by softmax_scale *
+ *     log2 e), whose finer significand keeps the rotation's rounding error
+ *     8x below bf16's; a rotated value beyond the fp16 range (65504) is
+ *     reported as MF_ERR_RANGE by mf_check.
+ *   - head_dim must be 64 or 128 (MF_ERR_UNSUPPORTED otherwise).
+ */
+#ifndef MF_H_
+#define MF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MF_API __attribute__((visibility("default")))
+#else
+#define MF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MF_OK = 0,
+  MF_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misaligned pointer, short workspace */
+  MF_ERR_UNSUPPORTED = 2, /* head_dim not 64/128, too many samples, grid side > 1024 */
+  MF_ERR_BUDGET = 3,      /* not even the first sample fits the token budget */
+  MF_ERR_CUDA = 4,        /* a CUDA call failed; see mf_last_cuda_error() */
+  MF_ERR_TIMEOUT = 5,     /* a kernel's bounded wait expired (reported by mf_check) */
+  MF_ERR_RANGE = 6        /* a rotated, scaled Q or K value left the fp16 range of the
+                             logit MMA (|value| > 65504; reported by mf_check) */
+} mf_status;
+
+/* One sample of a pack: text length in tokens, image height and width in
+ * pixels (positive multiples of 16). */
+typedef struct {
+  int32_t text_len;
+  int32_t height;
+  int32_t width;
+} mf_sample;
+
+/* Largest supported pack (samples) and latent grid side. */
+#define MF_MAX_SAMPLES 4096
+#define MF_MAX_GRID 1024
+/* Rows per attention tile; the work list counts tiles of this size. */
+#define MF_TILE 128
+
+/* A pack plan.  Filled by mf_pack_plan; every pointer points into the
+ * caller's plan workspace (device memory) and stays valid as long as it. */
+typedef struct {
+  int32_t n_samples;    /* samples packed: the longest prefix within the budget */
+  int32_t total_tokens; /* cu_seqlens[n_samples] */
+  int32_t max_seqlen;   /* max_i L_i */
+  int32_t max_grid;     /* max_i max(H_i/16, W_i/16) */
+  int32_t head_dim;     /* head_dim the RoPE table was built for */
+  int32_t n_tiles;      /* sum_i ceil(L_i / MF_TILE) */
+  int32_t *cu_seqlens;  /* device int32 [n_samples + 1], exclusive scan of L_i */
+  int32_t *pos;         /* device int32 [total_tokens][2]: (row, col); text = (-1, -1) */
+  float *rope_cs;       /* device float32 [max_grid][head_dim/4][2]: cos, sin of p*f_i */
+  int32_t *order;       /* device int32 [n_samples][2]: (sample, first tile), longest sample first */
+  int32_t *status;      /* device int32 status word written by kernels that time out */
+} mf_plan;
+
+/* Bytes of device workspace mf_pack_plan needs for this request.  Validates
+ * the request like mf_pack_plan (same error codes); `samples` is host memory. */
+MF_API mf_status mf_pack_plan_workspace_size(const mf_sample *samples, int32_t n_samples,
+                                      int32_t token_budget, int32_t head_dim, size_t *bytes);
+
+/* Plan a pack (review, section "Native-Resolution MMDiT": variable-length
+ * latent token rows packed under a fixed token budget, unpadded text, per-
+ * sample cumulative offsets).  The longest prefix of `samples` whose total
+ * token count is <= token_budget is packed (token_budget 0 = no budget).
+ *   samples      host array [n_samples]; 0 <= n_samples <= MF_MAX_SAMPLES
+ *   head_dim     64 or 128 (sizes the RoPE table)
+ *   rope_theta   RoPE base (> 0; 10000 is the usual value)
+ *   workspace    device memory of at least mf_pack_plan_workspace_size bytes,
+ *                256-byte aligned
+ *   plan_out     host struct, filled on success
+ * Runs a device prefix scan, the per-token id expansion and the RoPE table on
+ * `stream`, then synchronizes `stream` once to read the scalars back.
+ * Errors: MF_ERR_INVALID_ARG (null pointer, text_len < 0, H or W not a
+ * positive multiple of 16, total tokens >= 2^31, short or misaligned
+ * workspace), MF_ERR_UNSUPPORTED, MF_ERR_BUDGET, MF_ERR_CUDA. */
+MF_API mf_status mf_pack_plan(const mf_sample *samples, int32_t n_samples, int32_t token_budget,
+                       int32_t head_dim, float rope_theta, void *workspace,
+                       size_t workspace_bytes, mf_plan *plan_out, void *stream);
+
+/* Forward: for every sample i and head h,
+ *   O = softmax(s * R(Q) R(K)^T) V,  LSE = logsumexp(s * R(Q) R(K)^T)  (rows)
+ * over that sample's tokens only, R = the 2D rotation above.
+ *   q, k, v   device bf16 [plan->total_tokens, heads, head_dim]
+ *   o         device bf16, same shape (written)
+ *   lse       device float32 [heads, plan->total_tokens] (written)
+ * Errors: MF_ERR_INVALID_ARG (null/misaligned pointer, heads < 1, head_dim
+ * different from the plan's), MF_ERR_UNSUPPORTED, MF_ERR_CUDA. */
+MF_API mf_status mf_attn_fwd(const void *q, const void *k, const void *v, const mf_plan *plan,
+                      int32_t heads, int32_t head_dim, float softmax_scale, void *o,
+                      float *lse, void *stream);
+
+/* Bytes of device workspace mf_attn_bwd needs: float32 row dots
+ * D = rowsum(dO * O) [heads, total_tokens] and a float32 dQ accumulator
+ * [total_tokens, heads, head_dim]. */
+MF_API mf_status mf_attn_bwd_workspace_size(int32_t total_tokens, int32_t heads, int32_t head_dim,
+                                     size_t *bytes);
+
+/* Backward of mf_attn_fwd with respect to the un-rotated inputs:
+ *   P = exp(s R(Q) R(K)^T - LSE);  dV = P^T dO;  dP = dO V^T;
+ *   D = rowsum(dO * O);  dS = P * (dP - D);
+ *   dQ = R^T (s dS R(K));  dK = R^T (s dS^T R(Q))
+ *   q, k, v, o, dout  device bf16 [total_tokens, heads, head_dim]
+ *   lse               device float32 [heads, total_tokens] from mf_attn_fwd
+ *   workspace         device memory of mf_attn_bwd_workspace_size bytes,
+ *                     256-byte aligned (contents on entry are ignored)
+ *   dq, dk, dv        device bf16 [total_tokens, heads, head_dim] (written)
+ * Errors as mf_attn_fwd, plus a short workspace (MF_ERR_INVALID_ARG). */
+MF_API mf_status mf_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dout, const mf_plan *plan, int32_t heads,
+                      int32_t head_dim, float softmax_scale, void *workspace,
+                      size_t workspace_bytes, void *dq, void *dk, void *dv, void *stream);
+
+/* Synchronize `stream`, then read and clear the plan's device status word:
+ * MF_OK, MF_ERR_TIMEOUT, MF_ERR_RANGE, or MF_ERR_CUDA for a failed
+ * synchronization. */
+MF_API mf_status mf_check(const mf_plan *plan, void *stream);
+
+/* Static description of a status code. */
+MF_API const char *mf_status_string(mf_status status);
+
+/* Message of the last CUDA error seen by this thread ("" if none). */
+MF_API const char *mf_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MF_H_ */

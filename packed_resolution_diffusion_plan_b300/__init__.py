@@ -1,0 +1,224 @@
+"""Packed native-resolution joint attention for B300 -- Python binding.
+
+A thin ctypes layer over ``libmf.so`` (declared in ``include/mf.h``): it
+marshals arguments and allocates caller-side buffers with PyTorch; every step
+of the computation runs in the library's CUDA kernels.  There is no CPU path:
+if the library is missing or fails to load, every call raises.
+
+    plan = pack_plan([(text_len, height_px, width_px), ...], token_budget=32768)
+    o, lse = attn_fwd(q, k, v, plan)               # bf16 [T, heads, head_dim]
+    dq, dk, dv = attn_bwd(q, k, v, o, lse, do, plan)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["MfError", "Plan", "pack_plan", "attn_fwd", "attn_bwd", "check", "lib", "library_path",
+           "EXPORTED_SYMBOLS", "STATUS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libmf.so")
+
+STATUS = {0: "MF_OK", 1: "MF_ERR_INVALID_ARG", 2: "MF_ERR_UNSUPPORTED", 3: "MF_ERR_BUDGET",
+          4: "MF_ERR_CUDA", 5: "MF_ERR_TIMEOUT", 6: "MF_ERR_RANGE"}
+
+EXPORTED_SYMBOLS = ["mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd",
+                    "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_status_string",
+                    "mf_last_cuda_error"]
+
+TILE = 128
+
+
+class MfSample(ctypes.Structure):
+    _fields_ = [("text_len", ctypes.c_int32), ("height", ctypes.c_int32), ("width", ctypes.c_int32)]
+
+
+class MfPlan(ctypes.Structure):
+    _fields_ = [("n_samples", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("max_seqlen", ctypes.c_int32), ("max_grid", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
+                ("cu_seqlens", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("rope_cs", ctypes.c_void_p), ("order", ctypes.c_void_p),
+                ("status", ctypes.c_void_p)]
+
+
+class MfError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        self.code = STATUS.get(status, str(status))
+        msg = f"{where}: {self.code}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def lib():
+    """Load libmf.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise RuntimeError(f"libmf.so not found at {library_path}: build it with "
+                           "`python -m packed_resolution_diffusion_plan_b300.build`")
+    L = ctypes.CDLL(library_path)
+    c_i32, c_vp, c_sz = ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+    L.mf_pack_plan_workspace_size.argtypes = [ctypes.POINTER(MfSample), c_i32, c_i32, c_i32,
+                                              ctypes.POINTER(c_sz)]
+    L.mf_pack_plan.argtypes = [ctypes.POINTER(MfSample), c_i32, c_i32, c_i32, ctypes.c_float, c_vp,
+                               c_sz, ctypes.POINTER(MfPlan), c_vp]
+    L.mf_attn_fwd.argtypes = [c_vp, c_vp, c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32, ctypes.c_float,
+                              c_vp, c_vp, c_vp]
+    L.mf_attn_bwd_workspace_size.argtypes = [c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]
+    L.mf_attn_bwd.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32,
+                              ctypes.c_float, c_vp, c_sz, c_vp, c_vp, c_vp, c_vp]
+    L.mf_check.argtypes = [ctypes.POINTER(MfPlan), c_vp]
+    L.mf_status_string.argtypes = [c_i32]
+    L.mf_status_string.restype = ctypes.c_char_p
+    L.mf_last_cuda_error.argtypes = []
+    L.mf_last_cuda_error.restype = ctypes.c_char_p
+    for name in ("mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd",
+                 "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check"):
+        getattr(L, name).restype = c_i32
+    _lib = L
+    return L
+
+
+def _raise(status: int, where: str):
+    if status != 0:
+        detail = lib().mf_last_cuda_error().decode() if status == 4 else ""
+        raise MfError(status, where, detail)
+
+
+def _stream_ptr(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _samples_array(samples):
+    arr = (MfSample * max(1, len(samples)))()
+    for i, (t, h, w) in enumerate(samples):
+        arr[i] = MfSample(int(t), int(h), int(w))
+    return arr
+
+
+class Plan:
+    """A pack plan living in a device workspace owned by this object."""
+
+    def __init__(self, raw: MfPlan, workspace: torch.Tensor, samples, token_budget):
+        self.raw = raw
+        self.workspace = workspace
+        self.samples = list(samples)
+        self.token_budget = token_budget
+
+    n_samples = property(lambda self: self.raw.n_samples)
+    total_tokens = property(lambda self: self.raw.total_tokens)
+    max_seqlen = property(lambda self: self.raw.max_seqlen)
+    max_grid = property(lambda self: self.raw.max_grid)
+    head_dim = property(lambda self: self.raw.head_dim)
+    n_tiles = property(lambda self: self.raw.n_tiles)
+
+    @property
+    def device(self):
+        return self.workspace.device
+
+    def _view(self, ptr, count, dtype):
+        off = ptr - self.workspace.data_ptr()
+        nbytes = count * torch.empty((), dtype=dtype).element_size()
+        return self.workspace[off:off + nbytes].view(dtype)
+
+    def cu_seqlens(self) -> torch.Tensor:
+        return self._view(self.raw.cu_seqlens, self.n_samples + 1, torch.int32)
+
+    def pos(self) -> torch.Tensor:
+        return self._view(self.raw.pos, 2 * self.total_tokens, torch.int32).view(-1, 2)
+
+    def rope_table(self) -> torch.Tensor:
+        n = self.max_grid * (self.head_dim // 4) * 2
+        return self._view(self.raw.rope_cs, n, torch.float32).view(self.max_grid, self.head_dim // 4, 2)
+
+    def order(self) -> torch.Tensor:
+        return self._view(self.raw.order, 2 * self.n_samples, torch.int32).view(-1, 2)
+
+
+def pack_plan(samples, token_budget: int = 0, head_dim: int = 128, rope_theta: float = 10000.0,
+              device=None, stream=None) -> Plan:
+    """Plan a pack of (text_len, height_px, width_px) samples on the GPU."""
+    L = lib()
+    device = torch.device(device if device is not None else "cuda")
+    arr = _samples_array(samples)
+    nbytes = ctypes.c_size_t(0)
+    _raise(L.mf_pack_plan_workspace_size(arr, len(samples), int(token_budget), int(head_dim),
+                                         ctypes.byref(nbytes)), "mf_pack_plan_workspace_size")
+    ws = torch.empty(max(256, nbytes.value), dtype=torch.uint8, device=device)
+    raw = MfPlan()
+    _raise(L.mf_pack_plan(arr, len(samples), int(token_budget), int(head_dim), float(rope_theta),
+                          ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.byref(raw),
+                          _stream_ptr(stream, device)), "mf_pack_plan")
+    return Plan(raw, ws, samples, token_budget)
+
+
+def _check_qkv(plan: Plan, *ts):
+    for t in ts:
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous bf16 CUDA tensors [T, heads, head_dim]")
+        if t.dim() != 3 or t.shape[0] != plan.total_tokens or t.shape[2] != plan.head_dim:
+            raise ValueError(f"expected [{plan.total_tokens}, heads, {plan.head_dim}], got {tuple(t.shape)}")
+        if t.shape != ts[0].shape:
+            raise ValueError("shape mismatch")
+
+
+def attn_fwd(q, k, v, plan: Plan, softmax_scale: float = 0.0, out=None, lse=None, stream=None):
+    """O, LSE of packed 2D-RoPE joint attention (see mf_attn_fwd)."""
+    _check_qkv(plan, q, k, v)
+    T, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    _raise(lib().mf_attn_fwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                             ctypes.c_void_p(v.data_ptr()), ctypes.byref(plan.raw), H, D,
+                             float(softmax_scale), ctypes.c_void_p(out.data_ptr()),
+                             ctypes.c_void_p(lse.data_ptr()), _stream_ptr(stream, q.device)),
+           "mf_attn_fwd")
+    return out, lse
+
+
+def bwd_workspace_bytes(total_tokens: int, heads: int, head_dim: int) -> int:
+    n = ctypes.c_size_t(0)
+    _raise(lib().mf_attn_bwd_workspace_size(total_tokens, heads, head_dim, ctypes.byref(n)),
+           "mf_attn_bwd_workspace_size")
+    return n.value
+
+
+def attn_bwd(q, k, v, o, lse, do, plan: Plan, softmax_scale: float = 0.0, workspace=None,
+             dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV of packed 2D-RoPE joint attention (see mf_attn_bwd)."""
+    _check_qkv(plan, q, k, v, o, do)
+    T, H, D = q.shape
+    nbytes = bwd_workspace_bytes(T, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(256, nbytes), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    _raise(lib().mf_attn_bwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(o.data_ptr()),
+                             ctypes.c_void_p(lse.data_ptr()), ctypes.c_void_p(do.data_ptr()),
+                             ctypes.byref(plan.raw), H, D, float(softmax_scale),
+                             ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                             ctypes.c_void_p(dq.data_ptr()), ctypes.c_void_p(dk.data_ptr()),
+                             ctypes.c_void_p(dv.data_ptr()), _stream_ptr(stream, q.device)),
+           "mf_attn_bwd")
+    return dq, dk, dv
+
+
+def check(plan: Plan, stream=None):
+    """Synchronize and raise MfError(MF_ERR_TIMEOUT) if a kernel gave up a wait."""
+    _raise(lib().mf_check(ctypes.byref(plan.raw), _stream_ptr(stream, plan.device)), "mf_check")

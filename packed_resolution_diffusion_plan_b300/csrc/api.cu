@@ -1,0 +1,325 @@
+// C-ABI entry points of libmf (declared in include/mf.h): argument checks,
+// workspace layout, TMA descriptor encoding and kernel launches.  No device
+// memory is allocated here; every buffer comes from the caller.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/mf.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace {
+
+using mf::PlanScalars;
+
+thread_local std::string g_last_cuda_error;
+
+mf_status cuda_fail(cudaError_t e, const char* where) {
+  char buf[256];
+  snprintf(buf, sizeof(buf), "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+  g_last_cuda_error = buf;
+  return MF_ERR_CUDA;
+}
+
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- plan
+struct PlanLayout {
+  size_t off_scalars, off_samples, off_cu, off_order, off_pos, off_rope, bytes;
+  int32_t token_bound, grid_bound;
+};
+
+mf_status check_samples(const mf_sample* samples, int32_t n, int32_t budget, int32_t head_dim,
+                        PlanLayout* L) {
+  if (n < 0 || (n > 0 && samples == nullptr) || budget < 0) return MF_ERR_INVALID_ARG;
+  if (n > MF_MAX_SAMPLES) return MF_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
+  long long used = 0;
+  int32_t gmax = 0;
+  bool stopped = false;
+  for (int32_t i = 0; i < n; ++i) {
+    const mf_sample& s = samples[i];
+    if (s.text_len < 0 || s.height <= 0 || s.width <= 0 || (s.height % 16) || (s.width % 16))
+      return MF_ERR_INVALID_ARG;
+    const long long gh = s.height / 16, gw = s.width / 16;
+    if (gh > MF_MAX_GRID || gw > MF_MAX_GRID) return MF_ERR_UNSUPPORTED;
+    gmax = static_cast<int32_t>(std::max<long long>(gmax, std::max(gh, gw)));
+    const long long len = s.text_len + gh * gw;
+    if (!stopped) {
+      if (budget > 0 && used + len > budget) {
+        stopped = true;
+        if (i == 0) return MF_ERR_BUDGET;
+      } else {
+        used += len;
+        if (used >= (1ll << 31)) return MF_ERR_INVALID_ARG;
+      }
+    }
+  }
+  L->token_bound = static_cast<int32_t>(used);
+  L->grid_bound = gmax;
+  size_t off = 0;
+  L->off_scalars = off;
+  off = align_up(off + sizeof(PlanScalars), 256);
+  L->off_samples = off;
+  off = align_up(off + static_cast<size_t>(n) * 3 * sizeof(int32_t), 256);
+  L->off_cu = off;
+  off = align_up(off + static_cast<size_t>(n + 1) * sizeof(int32_t), 256);
+  L->off_order = off;
+  off = align_up(off + static_cast<size_t>(n) * 2 * sizeof(int32_t), 256);
+  L->off_pos = off;
+  off = align_up(off + static_cast<size_t>(L->token_bound) * 2 * sizeof(int32_t), 256);
+  L->off_rope = off;
+  off = align_up(off + static_cast<size_t>(gmax) * (head_dim / 4) * 2 * sizeof(float), 256);
+  L->bytes = off;
+  return MF_OK;
+}
+
+// ---------------------------------------------------------------- TMA
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// [rows, heads*head_dim] bf16 view of a [T, heads, head_dim] tensor; boxes of
+// 128 rows x 64 columns, 128-byte swizzle, zero fill past the last row.
+mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t heads, int32_t head_dim) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    g_last_cuda_error = "cuTensorMapEncodeTiled entry point not available";
+    return MF_ERR_CUDA;
+  }
+  const cuuint64_t cols = static_cast<cuuint64_t>(heads) * head_dim;
+  cuuint64_t gdim[2] = {cols, static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {cols * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mf::kTile)};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[128];
+    snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed with CUresult %d", static_cast<int>(r));
+    g_last_cuda_error = buf;
+    return MF_ERR_CUDA;
+  }
+  return MF_OK;
+}
+
+mf_status check_attn_common(const mf_plan* plan, int32_t heads, int32_t head_dim) {
+  if (plan == nullptr || heads < 1) return MF_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
+  if (head_dim != plan->head_dim) return MF_ERR_INVALID_ARG;
+  if (plan->total_tokens < 0 || plan->n_samples < 0) return MF_ERR_INVALID_ARG;
+  if (plan->total_tokens > 0 &&
+      (plan->cu_seqlens == nullptr || plan->pos == nullptr || plan->rope_cs == nullptr ||
+       plan->order == nullptr || plan->status == nullptr))
+    return MF_ERR_INVALID_ARG;
+  if (static_cast<long long>(plan->n_tiles) * heads >= (1ll << 31)) return MF_ERR_UNSUPPORTED;
+  return MF_OK;
+}
+
+mf::AttnGeom make_geom(const mf_plan* plan, int32_t heads) {
+  mf::AttnGeom g;
+  g.cu_seqlens = plan->cu_seqlens;
+  g.pos = plan->pos;
+  g.rope_cs = plan->rope_cs;
+  g.order = plan->order;
+  g.n_samples = plan->n_samples;
+  g.total_tokens = plan->total_tokens;
+  g.heads = heads;
+  g.n_items = plan->n_tiles * heads;
+  g.status = plan->status;
+  return g;
+}
+
+float resolve_scale(float s, int32_t head_dim) {
+  return (s > 0.f && std::isfinite(s)) ? s : 1.0f / std::sqrt(static_cast<float>(head_dim));
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" {
+
+mf_status mf_pack_plan_workspace_size(const mf_sample* samples, int32_t n_samples, int32_t token_budget,
+                                      int32_t head_dim, size_t* bytes) {
+  if (bytes == nullptr) return MF_ERR_INVALID_ARG;
+  PlanLayout L;
+  mf_status st = check_samples(samples, n_samples, token_budget, head_dim, &L);
+  if (st != MF_OK) return st;
+  *bytes = L.bytes;
+  return MF_OK;
+}
+
+mf_status mf_pack_plan(const mf_sample* samples, int32_t n_samples, int32_t token_budget, int32_t head_dim,
+                       float rope_theta, void* workspace, size_t workspace_bytes, mf_plan* plan_out,
+                       void* stream) {
+  if (plan_out == nullptr || workspace == nullptr) return MF_ERR_INVALID_ARG;
+  if (!(rope_theta > 0.f) || !std::isfinite(rope_theta)) return MF_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MF_ERR_INVALID_ARG;
+  PlanLayout L;
+  mf_status st = check_samples(samples, n_samples, token_budget, head_dim, &L);
+  if (st != MF_OK) return st;
+  if (workspace_bytes < L.bytes) return MF_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  mf::PlanArgs a;
+  a.samples = reinterpret_cast<const int32_t*>(ws + L.off_samples);
+  a.n = n_samples;
+  a.budget = token_budget;
+  a.scalars = reinterpret_cast<PlanScalars*>(ws + L.off_scalars);
+  a.cu_seqlens = reinterpret_cast<int32_t*>(ws + L.off_cu);
+  a.order = reinterpret_cast<int32_t*>(ws + L.off_order);
+  a.pos = reinterpret_cast<int32_t*>(ws + L.off_pos);
+  a.token_bound = L.token_bound;
+  a.rope_cs = reinterpret_cast<float*>(ws + L.off_rope);
+  a.grid_bound = L.grid_bound;
+  a.head_dim = head_dim;
+  a.theta = rope_theta;
+  cudaError_t e;
+  if (n_samples > 0) {
+    e = cudaMemcpyAsync(ws + L.off_samples, samples, static_cast<size_t>(n_samples) * sizeof(mf_sample),
+                        cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mf_pack_plan: copy samples");
+  }
+  e = mf::launch_pack_plan(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "mf_pack_plan: launch");
+  PlanScalars sc;
+  e = cudaMemcpyAsync(&sc, ws + L.off_scalars, sizeof(sc), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "mf_pack_plan: read scalars");
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "mf_pack_plan: synchronize");
+  plan_out->n_samples = sc.n_packed;
+  plan_out->total_tokens = sc.total_tokens;
+  plan_out->max_seqlen = sc.max_seqlen;
+  plan_out->max_grid = sc.max_grid;
+  plan_out->head_dim = head_dim;
+  plan_out->n_tiles = sc.n_tiles;
+  plan_out->cu_seqlens = a.cu_seqlens;
+  plan_out->pos = a.pos;
+  plan_out->rope_cs = a.rope_cs;
+  plan_out->order = a.order;
+  plan_out->status = &a.scalars->status;
+  return MF_OK;
+}
+
+mf_status mf_attn_fwd(const void* q, const void* k, const void* v, const mf_plan* plan, int32_t heads,
+                      int32_t head_dim, float softmax_scale, void* o, float* lse, void* stream) {
+  mf_status st = check_attn_common(plan, heads, head_dim);
+  if (st != MF_OK) return st;
+  if (plan->total_tokens == 0) return MF_OK;
+  if (!q || !k || !v || !o || !lse) return MF_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return MF_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv;
+  if ((st = make_tmap(&tq, q, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tk, k, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  mf::FwdArgs a;
+  a.g = make_geom(plan, heads);
+  a.scale_log2 = resolve_scale(softmax_scale, head_dim) * kLog2e;
+  a.o = o;
+  a.lse = lse;
+  cudaError_t e = mf::launch_attn_fwd(a, tq, tk, tv, head_dim, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mf_attn_fwd");
+  return MF_OK;
+}
+
+mf_status mf_attn_bwd_workspace_size(int32_t total_tokens, int32_t heads, int32_t head_dim, size_t* bytes) {
+  if (bytes == nullptr || total_tokens < 0 || heads < 1) return MF_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
+  const size_t rows = static_cast<size_t>(total_tokens) * heads;
+  *bytes = align_up(rows * sizeof(float), 256) + align_up(rows * head_dim * sizeof(float), 256);
+  return MF_OK;
+}
+
+mf_status mf_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, const mf_plan* plan, int32_t heads, int32_t head_dim,
+                      float softmax_scale, void* workspace, size_t workspace_bytes, void* dq, void* dk,
+                      void* dv, void* stream) {
+  mf_status st = check_attn_common(plan, heads, head_dim);
+  if (st != MF_OK) return st;
+  if (plan->total_tokens == 0) return MF_OK;
+  if (!q || !k || !v || !o || !lse || !dout || !workspace || !dq || !dk || !dv) return MF_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return MF_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MF_ERR_INVALID_ARG;
+  size_t need = 0;
+  if ((st = mf_attn_bwd_workspace_size(plan->total_tokens, heads, head_dim, &need)) != MF_OK) return st;
+  if (workspace_bytes < need) return MF_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = make_tmap(&tq, q, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tk, k, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tdo, dout, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  const size_t rows = static_cast<size_t>(plan->total_tokens) * heads;
+  mf::BwdArgs a;
+  a.g = make_geom(plan, heads);
+  a.scale = resolve_scale(softmax_scale, head_dim);
+  a.scale_log2 = a.scale * kLog2e;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dsum = static_cast<float*>(workspace);
+  a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align_up(rows * sizeof(float), 256));
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  cudaError_t e = mf::launch_attn_bwd(a, tq, tk, tv, tdo, head_dim, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mf_attn_bwd");
+  return MF_OK;
+}
+
+mf_status mf_check(const mf_plan* plan, void* stream) {
+  if (plan == nullptr || plan->status == nullptr) return MF_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "mf_check: synchronize");
+  int32_t status = 0;
+  e = cudaMemcpyAsync(&status, plan->status, sizeof(status), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "mf_check: read status");
+  if (status != 0) {
+    e = cudaMemsetAsync(plan->status, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "mf_check: clear status");
+    return (status & mf::kStatusTimeout) ? MF_ERR_TIMEOUT : MF_ERR_RANGE;
+  }
+  return MF_OK;
+}
+
+const char* mf_status_string(mf_status status) {
+  switch (status) {
+    case MF_OK: return "ok";
+    case MF_ERR_INVALID_ARG: return "invalid argument";
+    case MF_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MF_ERR_BUDGET: return "first sample exceeds the token budget";
+    case MF_ERR_CUDA: return "CUDA error";
+    case MF_ERR_TIMEOUT: return "a kernel wait timed out";
+    case MF_ERR_RANGE: return "a rotated Q/K value exceeded the fp16 range of the logit product";
+  }
+  return "unknown status";
+}
+
+const char* mf_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+}  // extern "C"

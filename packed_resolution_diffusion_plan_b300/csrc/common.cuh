@@ -1,0 +1,86 @@
+// Parameter blocks and launch declarations shared by the C-ABI layer and the
+// kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace mf {
+
+constexpr int kTile = 128;            // rows per Q tile and per KV tile
+constexpr int kPlanThreads = 1024;    // one CTA runs the pack scan
+constexpr int kPlanMaxSamples = 4096;
+
+// Scalars the pack-plan kernel writes for the host (one 32-byte block).
+struct PlanScalars {
+  int32_t n_packed;
+  int32_t total_tokens;
+  int32_t max_seqlen;
+  int32_t max_grid;
+  int32_t n_tiles;
+  int32_t status;
+  int32_t pad[2];
+};
+
+struct PlanArgs {
+  const int32_t* samples;   // device [n][3] (text_len, height_px, width_px)
+  int32_t n;
+  int32_t budget;           // 0 = none
+  PlanScalars* scalars;
+  int32_t* cu_seqlens;      // [n+1]
+  int32_t* order;           // [n][2]
+  int32_t* pos;             // [token_bound][2]
+  int32_t token_bound;
+  float* rope_cs;           // [grid_bound][head_dim/4][2]
+  int32_t grid_bound;
+  int32_t head_dim;
+  float theta;
+};
+
+cudaError_t launch_pack_plan(const PlanArgs& a, cudaStream_t stream);
+
+// Attention work decode: the plan's order list holds, per sample sorted by
+// length (longest first), the sample index and its first tile index in that
+// order; a CTA item is (sorted sample, head, tile) with tiles fastest.
+struct AttnGeom {
+  const int32_t* cu_seqlens;
+  const int32_t* pos;
+  const float* rope_cs;
+  const int32_t* order;
+  int32_t n_samples;
+  int32_t total_tokens;
+  int32_t heads;
+  int32_t n_items;          // n_tiles * heads
+  int32_t* status;
+};
+
+struct FwdArgs {
+  AttnGeom g;
+  float scale_log2;          // softmax_scale * log2(e), folded into the fp16 Q operand
+  void* o;                   // bf16 [T, heads, D]
+  float* lse;                // [heads, T]
+};
+
+cudaError_t launch_attn_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, int head_dim, cudaStream_t stream);
+
+struct BwdArgs {
+  AttnGeom g;
+  float scale;               // softmax_scale
+  float scale_log2;          // softmax_scale * log2(e)
+  const void* o;
+  const void* dout;
+  const float* lse;
+  float* dsum;               // [heads, T] rowsum(dO * O)
+  float* dq_acc;             // [T, heads, D] float32 accumulator (zeroed by the preprocess)
+  void* dq;
+  void* dk;
+  void* dv;
+};
+
+cudaError_t launch_attn_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, int head_dim,
+                            cudaStream_t stream);
+
+}  // namespace mf
