@@ -38,7 +38,9 @@ def assert_close(name, got, want, kind, factor=1.0):
     tol = {k: v * factor for k, v in TOL[kind].items()}
     mab = float(np.abs(got - want).max()) if got.size else 0.0
     assert mab <= tol["max_abs"], f"{name}: max-abs {mab:.3e} > {tol['max_abs']}"
-    if "rel_l2" in tol and got.size:
+    # relative L2 is undefined against an all-zero reference (e.g. dQ, dK of a
+    # one-token sample, whose softmax is constant); max-abs still applies.
+    if "rel_l2" in tol and got.size and np.linalg.norm(want) > 0:
         r = rel_l2(got, want)
         assert r <= tol["rel_l2"], f"{name}: rel-L2 {r:.3e} > {tol['rel_l2']}"
     return mab

@@ -1,0 +1,103 @@
+"""mf_attn_bwd on the GPU vs the float64 oracle.  The GPU backward consumes
+the GPU forward's O and LSE; the oracle computes its own from the same bf16
+Q, K, V, dO, so the comparison covers forward + backward end to end."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import packed_resolution_diffusion_plan_b300 as mf
+import synth
+from _parity import assert_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_fwd_bwd(samples, heads, head_dim, seed, budget=0, scale=0.0):
+    wl = synth.Workload("t", samples, heads, head_dim, "fwd+bwd", token_budget=budget, seed=seed)
+    t = synth.draw_tensors(wl, with_grad=True)
+    plan = mf.pack_plan(samples, token_budget=budget, head_dim=head_dim)
+    T = plan.total_tokens
+    q, k, v, do = (t[n][:T].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = mf.attn_fwd(q, k, v, plan, softmax_scale=scale)
+    dq, dk, dv = mf.attn_bwd(q, k, v, o, lse, do, plan, softmax_scale=scale)
+    mf.check(plan)
+    return plan, (q, k, v, do), (dq, dk, dv)
+
+
+def _run_full(samples, heads, head_dim, seed, budget=0, scale=0.0):
+    plan, (q, k, v, do), (dq, dk, dv) = _gpu_fwd_bwd(samples, heads, head_dim, seed, budget, scale)
+    ref = oracle.pack_plan(samples, budget)
+    cu, pos = ref["cu_seqlens"], ref["pos"]
+    qn, kn, vn, gn = to64(q), to64(k), to64(v), to64(do)
+    O, L = oracle.attn_fwd(qn, kn, vn, cu, pos, softmax_scale=scale)
+    rq, rk, rv = oracle.attn_bwd(qn, kn, vn, O, L, gn, cu, pos, softmax_scale=scale)
+    assert_close("dV", to64(dv), rv, "grad")
+    assert_close("dK", to64(dk), rk, "grad")
+    assert_close("dQ", to64(dq), rq, "grad")
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_bwd_tiny(seed):
+    wl = synth.tiny(seed)
+    _run_full(wl.samples, wl.heads, wl.head_dim, seed)
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("seed", range(2))
+def test_bwd_ragged_multi_tile(head_dim, seed):
+    samples = [(0, 16, 16), (7, 64, 32), (0, 128, 128), (200, 160, 48), (1, 16, 16), (55, 96, 208)]
+    rng = np.random.default_rng(seed)
+    rng.shuffle(samples)
+    _run_full(samples, heads=3, head_dim=head_dim, seed=seed)
+
+
+@pytest.mark.parametrize("L", [1, 127, 128, 129, 256, 300])
+def test_bwd_tile_boundaries(L):
+    _run_full([(0, 16, 16 * L)], heads=2, head_dim=128, seed=L)
+
+
+def test_bwd_single_token_closed_form():
+    """One key: P = 1, dS = 0, so dQ = dK = 0 and dV = dO."""
+    plan, (q, k, v, do), (dq, dk, dv) = _gpu_fwd_bwd([(0, 16, 16), (1, 16, 16)], 2, 128, 3)
+    assert float(dq[0].abs().max()) < 1e-4 and float(dk[0].abs().max()) < 1e-4
+    assert torch.equal(dv[0], do[0])
+
+
+def test_bwd_budget_prefix():
+    _run_full([(30, 96, 96), (12, 64, 48), (0, 48, 160)], heads=2, head_dim=64, seed=6, budget=80)
+
+
+def test_bwd_empty_pack():
+    plan = mf.pack_plan([], 0)
+    z = torch.empty((0, 2, 64), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((2, 0), dtype=torch.float32, device="cuda")
+    plan_d = mf.pack_plan([], 0, head_dim=64)
+    dq, dk, dv = mf.attn_bwd(z, z, z, z, lse, z, plan_d)
+    mf.check(plan_d)
+    assert dq.shape == (0, 2, 64)
+
+
+@pytest.mark.parametrize("name,samples_idx", [("native_res_32k", [2, 5]), ("extreme_aspect", [0])])
+def test_bwd_full_size_per_sample(name, samples_idx):
+    """Full-size pack in the bench's launch configuration; the oracle recomputes
+    selected samples on a few heads (samples are independent, so a sample's
+    gradients depend only on its own rows)."""
+    wl = synth.WORKLOADS[name]()
+    plan, (q, k, v, do), (dq, dk, dv) = _gpu_fwd_bwd(wl.samples, wl.heads, wl.head_dim, wl.seed,
+                                                     wl.token_budget)
+    ref = oracle.pack_plan(wl.samples, wl.token_budget)
+    cu = ref["cu_seqlens"]
+    dq_c, dk_c, dv_c = to64(dq), to64(dk), to64(dv)
+    assert np.all(np.isfinite(dq_c)) and np.all(np.isfinite(dk_c)) and np.all(np.isfinite(dv_c))
+    for si in samples_idx:
+        a, b = int(cu[si]), int(cu[si + 1])
+        sub = oracle.pack_plan([wl.samples[si]])
+        for h in (0, wl.heads - 1):
+            hs = slice(h, h + 1)
+            qn, kn, vn, gn = (to64(x[a:b, hs]) for x in (q, k, v, do))
+            O, L = oracle.attn_fwd(qn, kn, vn, sub["cu_seqlens"], sub["pos"])
+            rq, rk, rv = oracle.attn_bwd(qn, kn, vn, O, L, gn, sub["cu_seqlens"], sub["pos"])
+            assert_close(f"dV[{name},s{si},h{h}]", dv_c[a:b, hs], rv, "grad")
+            assert_close(f"dK[{name},s{si},h{h}]", dk_c[a:b, hs], rk, "grad")
+            assert_close(f"dQ[{name},s{si},h{h}]", dq_c[a:b, hs], rq, "grad")
