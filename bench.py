@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Benchmark of the packed native-resolution attention hot path on B300.
+
+One step = the whole path over one synthetic pack: mf_pack_plan (device
+scan, per-token ids, RoPE table), mf_attn_fwd, mf_attn_bwd.  Throughput is
+reported as fwd+bwd TFLOP/s with FLOPs = 4*heads*head_dim*sum(L_i^2) forward
+and 2.5x that backward (algorithmic: only the per-sample blocks count).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mf|reference]
+
+N > 1 runs under torchrun: every rank plans and runs its own pack (same
+shapes, its own tensor values) -- packs are independent, so there is no
+exchange and scaling is weak.  Rank 0 prints one JSON line.
+
+`--impl reference` times the float64 CPU oracle (the only CPU code this
+benchmark may run) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "packed 2D-RoPE varlen attention fwd+bwd TFLOP/s; fraction of bf16 TC peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mf", "reference"], default="mf")
+    ap.add_argument("--workload", default="native_res_32k", choices=list(synth.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def pack_flops(samples, heads, head_dim):
+    lens = [t + (h // 16) * (w // 16) for (t, h, w) in samples]
+    s2 = float(sum(L * L for L in lens))
+    fwd = 4.0 * heads * head_dim * s2
+    return fwd, 2.5 * fwd, lens
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.path = None
+        self.gpu_id = None
+        try:
+            u = torch.cuda.get_device_properties(device).uuid
+            self.gpu_id = "GPU-" + str(u)
+        except Exception:
+            self.gpu_id = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# oracle (CPU) baseline
+# --------------------------------------------------------------------------
+
+def _blas_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return int(max(i.get("num_threads", 1) for i in info)) if info else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(wl, seconds, max_heads=None):
+    """Time the oracle's fwd+bwd on one sample of the workload, head after
+    head, until `seconds` of CPU work (or all heads) are done."""
+    import oracle
+    lens = [t + (h // 16) * (w // 16) for (t, h, w) in wl.samples]
+    # the sample whose length is closest to 3,600 tokens: large enough to be
+    # representative, small enough that one head takes about a second
+    si = int(np.argmin([abs(L - 3600) for L in lens]))
+    s = wl.samples[si]
+    p = oracle.pack_plan([s])
+    n = p["total_tokens"]
+    g = torch.Generator("cpu").manual_seed(wl.seed)
+    shape = (n, 1, wl.head_dim)
+    heads = 0
+    flop = 0.0
+    t0 = time.perf_counter()
+    while True:
+        q, k, v, do = (torch.randn(shape, generator=g).to(torch.bfloat16).double().numpy() for _ in range(4))
+        O, L = oracle.attn_fwd(q, k, v, p["cu_seqlens"], p["pos"])
+        oracle.attn_bwd(q, k, v, O, L, do, p["cu_seqlens"], p["pos"])
+        heads += 1
+        flop += 3.5 * 4.0 * wl.head_dim * n * n
+        el = time.perf_counter() - t0
+        if el >= seconds or heads >= (max_heads or wl.heads):
+            break
+    return {"value": flop / el / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "seconds": round(el, 3),
+            "sample": f"float64 oracle fwd+bwd of sample {si} ({n} tokens) of the {wl.name} pack, "
+                      f"{heads} head(s) x head_dim {wl.head_dim}"}
+
+
+# --------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    wl = synth.WORKLOADS[args.workload](args.seed)
+    for _ in range(args.warmup):
+        oracle_sample(wl, 0.0, max_heads=1)
+    t0 = time.perf_counter()
+    vals = []
+    last = None
+    for _ in range(args.steps):
+        last = oracle_sample(wl, 0.0, max_heads=1)
+        vals.append(last["value"])
+    el = time.perf_counter() - t0
+    value = float(np.mean(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{wl.name} seed {wl.seed}", "step": last["sample"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# the library arm
+# --------------------------------------------------------------------------
+
+def run_mf(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import packed_resolution_diffusion_plan_b300 as mf
+
+    wl = synth.WORKLOADS[args.workload](args.seed)
+    fwd_flop, bwd_flop, lens = pack_flops(wl.samples, wl.heads, wl.head_dim)
+    step_flop = fwd_flop + bwd_flop
+    wl_vals = synth.Workload(wl.name, wl.samples, wl.heads, wl.head_dim, wl.passes, wl.token_budget,
+                             wl.cfg_pairs, seed=args.seed + 1000 * rank)
+    host = synth.draw_tensors(wl_vals, with_grad=True)
+    T, H, D = host["q"].shape
+    q, k, v, do = (host[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(mf.bwd_workspace_bytes(T, H, D), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        plan = mf.pack_plan(wl.samples, token_budget=wl.token_budget, head_dim=D, device=dev)
+        if ev is not None:
+            mf.record_main_kernel(ev[0], ev[1])
+        mf.attn_fwd(q, k, v, plan, out=o, lse=lse)
+        if ev is not None:
+            mf.record_main_kernel(ev[2], ev[3])
+        mf.attn_bwd(q, k, v, o, lse, do, plan, workspace=ws, dq=dq, dk=dk, dv=dv)
+        return plan
+
+    for _ in range(max(args.warmup, 1)):
+        plan = step()
+    mf.check(plan)
+    launches_per_step = 3 + 1 + 3  # scan, ids, RoPE table; forward; bwd pre, main, dq
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        plan = step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    mf.check(plan)
+    ms_step = t_start.elapsed_time(t_end) / args.steps
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    bwd_main_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+    if dist:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * step_flop / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    pin = {n: host[n].pin_memory() for n in ("q", "k", "v", "do")}
+    out_h = {n: torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory() for n in ("o", "dq", "dk", "dv")}
+    lse_h = torch.empty((H, T), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_h.values()) + lse_h.numel() * 4
+
+    def e2e_step():
+        for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
+            dst.copy_(pin[n], non_blocking=True)
+        step()
+        for n, src in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+            out_h[n].copy_(src, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    mf.check(plan)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    kernels = {
+        "attn_fwd_kernel": {"ms": fwd_ms, "flop": fwd_flop},
+        "bwd_main_kernel": {"ms": bwd_main_ms, "flop": bwd_flop},
+    }
+    for kname, kd in kernels.items():
+        kd["tflops"] = kd["flop"] / (kd["ms"] * 1e-3) / 1e12
+        kd["frac_sustained"] = kd["tflops"] / peak
+        kd["frac_burst"] = kd["tflops"] / peak_burst
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    traffic = load_traffic(dom)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": kernels[dom]["tflops"], "peak": peak,
+                "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / peak, "traffic": traffic,
+                "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                "frac_of_burst_peak": kernels[dom]["tflops"] / peak_burst,
+                "per_kernel": {n: {k2: round(v2, 4) for k2, v2 in kd.items()} for n, kd in kernels.items()}}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(wl, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "precision": "bf16 inputs/outputs; tcgen05 MMAs with fp32 accumulation (logit products on fp16 "
+                     "copies of the rotated Q/K rows, P*V and dO products in bf16)",
+        "config": {"workload": f"{wl.name} seed {wl.seed}", "samples": [list(s) for s in wl.samples],
+                   "seq_lens": lens, "total_tokens": T, "heads": H, "head_dim": D,
+                   "token_budget": wl.token_budget, "fwd_tflop": fwd_flop / 1e12, "bwd_tflop": bwd_flop / 1e12,
+                   "step": "pack plan + forward + backward",
+                   "l2": f"no flush: Q/K/V/dO/O are {T * H * D * 2 / 1e6:.0f} MB each (> 126 MB L2)",
+                   "parallelism": f"{world} independent pack(s), one per GPU"},
+        "tokens_per_s": world * T / (ms_step * 1e-3),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * step_flop / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+KERNEL_SOURCES = {
+    "attn_fwd_kernel": ["attn_fwd.cu", "attn_common.cuh", "ptx.cuh", "common.cuh"],
+    "bwd_main_kernel": ["attn_bwd.cu", "attn_common.cuh", "ptx.cuh", "common.cuh"],
+}
+
+
+def kernel_source_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "packed_resolution_diffusion_plan_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from its committed ncu summary
+    (profiles/<kernel>_traffic.txt), or None when there is none or when the
+    kernel's sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    fields = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                key, val = line.split(":", 1)
+                fields[key.strip()] = val.strip()
+    if fields.get("source_hash") != kernel_source_hash(kernel):
+        return None
+    try:
+        return float(fields["bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_mf(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

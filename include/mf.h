@@ -166,6 +166,15 @@ MF_API mf_status mf_attn_bwd(const void *q, const void *k, const void *v, const 
  * synchronization. */
 MF_API mf_status mf_check(const mf_plan *plan, void *stream);
 
+/* Profiling aid: the next mf_attn_fwd or mf_attn_bwd call made by this
+ * thread records `start_event` on its stream right before its main attention
+ * kernel and `stop_event` right after it (cudaEvent_t handles created by the
+ * caller; both NULL clears the request).  The request is consumed by that
+ * one call.  This lets a caller time the tensor-core kernel alone, without
+ * the backward's pre- and post-processing kernels.  MF_ERR_INVALID_ARG if
+ * exactly one of the two is NULL. */
+MF_API mf_status mf_record_main_kernel(void *start_event, void *stop_event);
+
 /* Static description of a status code. */
 MF_API const char *mf_status_string(mf_status status);
 

@@ -16,7 +16,8 @@ import os
 
 import torch
 
-__all__ = ["MfError", "Plan", "pack_plan", "attn_fwd", "attn_bwd", "check", "lib", "library_path",
+__all__ = ["MfError", "Plan", "pack_plan", "attn_fwd", "attn_bwd", "check", "record_main_kernel", "lib",
+           "library_path",
            "EXPORTED_SYMBOLS", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -26,8 +27,8 @@ STATUS = {0: "MF_OK", 1: "MF_ERR_INVALID_ARG", 2: "MF_ERR_UNSUPPORTED", 3: "MF_E
           4: "MF_ERR_CUDA", 5: "MF_ERR_TIMEOUT", 6: "MF_ERR_RANGE"}
 
 EXPORTED_SYMBOLS = ["mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd",
-                    "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_status_string",
-                    "mf_last_cuda_error"]
+                    "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_record_main_kernel",
+                    "mf_status_string", "mf_last_cuda_error"]
 
 TILE = 128
 
@@ -78,12 +79,13 @@ def lib():
     L.mf_attn_bwd.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32,
                               ctypes.c_float, c_vp, c_sz, c_vp, c_vp, c_vp, c_vp]
     L.mf_check.argtypes = [ctypes.POINTER(MfPlan), c_vp]
+    L.mf_record_main_kernel.argtypes = [c_vp, c_vp]
     L.mf_status_string.argtypes = [c_i32]
     L.mf_status_string.restype = ctypes.c_char_p
     L.mf_last_cuda_error.argtypes = []
     L.mf_last_cuda_error.restype = ctypes.c_char_p
     for name in ("mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd",
-                 "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check"):
+                 "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_record_main_kernel"):
         getattr(L, name).restype = c_i32
     _lib = L
     return L
@@ -217,6 +219,23 @@ def attn_bwd(q, k, v, o, lse, do, plan: Plan, softmax_scale: float = 0.0, worksp
                              ctypes.c_void_p(dv.data_ptr()), _stream_ptr(stream, q.device)),
            "mf_attn_bwd")
     return dq, dk, dv
+
+
+def record_main_kernel(start=None, stop=None, stream=None):
+    """Have the next attn_fwd / attn_bwd call record torch.cuda.Event `start`
+    right before and `stop` right after its main tensor-core kernel.
+
+    Both events are first recorded here on `stream` so that torch considers
+    them recorded (it refuses elapsed_time otherwise); the library's own
+    record during the attention call then supersedes that placeholder."""
+    if start is not None and stop is not None:
+        st = stream if stream is not None else torch.cuda.current_stream()
+        start.record(st)
+        stop.record(st)
+        a, b = ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event)
+    else:
+        a = b = None
+    _raise(lib().mf_record_main_kernel(a, b), "mf_record_main_kernel")
 
 
 def check(plan: Plan, stream=None):

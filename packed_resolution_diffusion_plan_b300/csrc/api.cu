@@ -15,6 +15,15 @@ namespace {
 using mf::PlanScalars;
 
 thread_local std::string g_last_cuda_error;
+// One-shot event pair set by mf_record_main_kernel, consumed by the next
+// attention call on this thread.
+thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+
+void take_events(cudaEvent_t* a, cudaEvent_t* b) {
+  *a = g_ev_start;
+  *b = g_ev_stop;
+  g_ev_start = g_ev_stop = nullptr;
+}
 
 mf_status cuda_fail(cudaError_t e, const char* where) {
   char buf[256];
@@ -238,7 +247,9 @@ mf_status mf_attn_fwd(const void* q, const void* k, const void* v, const mf_plan
   a.scale_log2 = resolve_scale(softmax_scale, head_dim) * kLog2e;
   a.o = o;
   a.lse = lse;
-  cudaError_t e = mf::launch_attn_fwd(a, tq, tk, tv, head_dim, static_cast<cudaStream_t>(stream));
+  cudaEvent_t ev0, ev1;
+  take_events(&ev0, &ev1);
+  cudaError_t e = mf::launch_attn_fwd(a, tq, tk, tv, head_dim, static_cast<cudaStream_t>(stream), ev0, ev1);
   if (e != cudaSuccess) return cuda_fail(e, "mf_attn_fwd");
   return MF_OK;
 }
@@ -284,7 +295,9 @@ mf_status mf_attn_bwd(const void* q, const void* k, const void* v, const void* o
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  cudaError_t e = mf::launch_attn_bwd(a, tq, tk, tv, tdo, head_dim, static_cast<cudaStream_t>(stream));
+  cudaEvent_t ev0, ev1;
+  take_events(&ev0, &ev1);
+  cudaError_t e = mf::launch_attn_bwd(a, tq, tk, tv, tdo, head_dim, static_cast<cudaStream_t>(stream), ev0, ev1);
   if (e != cudaSuccess) return cuda_fail(e, "mf_attn_bwd");
   return MF_OK;
 }
@@ -304,6 +317,13 @@ mf_status mf_check(const mf_plan* plan, void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "mf_check: clear status");
     return (status & mf::kStatusTimeout) ? MF_ERR_TIMEOUT : MF_ERR_RANGE;
   }
+  return MF_OK;
+}
+
+mf_status mf_record_main_kernel(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return MF_ERR_INVALID_ARG;
+  g_ev_start = static_cast<cudaEvent_t>(start_event);
+  g_ev_stop = static_cast<cudaEvent_t>(stop_event);
   return MF_OK;
 }
 

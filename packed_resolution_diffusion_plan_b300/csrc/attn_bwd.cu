@@ -443,7 +443,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, cudaStream_t stream) {
+                         const CUtensorMap& tdo, cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
   using C = BwdCfg<D>;
   const long long chunks = static_cast<long long>(a.g.total_tokens) * a.g.heads * (D / 8);
   const int threads = 256;
@@ -453,9 +453,11 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
+  if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return e;
   bwd_main_kernel<D><<<a.g.n_items, kThreads, C::kDynSmem, stream>>>(tq, tk, tv, tdo, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return e;
   bwd_dq_kernel<D><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
   return cudaGetLastError();
 }
@@ -463,10 +465,11 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
 }  // namespace
 
 cudaError_t launch_attn_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, int head_dim, cudaStream_t stream) {
+                            const CUtensorMap& tdo, int head_dim, cudaStream_t stream,
+                            cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   if (a.g.n_items <= 0) return cudaSuccess;
-  if (head_dim == 128) return launch_bwd_d<128>(a, tq, tk, tv, tdo, stream);
-  return launch_bwd_d<64>(a, tq, tk, tv, tdo, stream);
+  if (head_dim == 128) return launch_bwd_d<128>(a, tq, tk, tv, tdo, stream, ev_start, ev_stop);
+  return launch_bwd_d<64>(a, tq, tk, tv, tdo, stream, ev_start, ev_stop);
 }
 
 }  // namespace mf

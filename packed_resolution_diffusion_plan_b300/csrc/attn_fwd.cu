@@ -322,21 +322,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
 template <int D>
 cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, cudaStream_t stream) {
+                         const CUtensorMap& tv, cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
   using C = FwdCfg<D>;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
+  if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return e;
   attn_fwd_kernel<D><<<a.g.n_items, kThreads, C::kDynSmem, stream>>>(tq, tk, tv, a);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, stream);
+  return e;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, int head_dim, cudaStream_t stream) {
+                            const CUtensorMap& tv, int head_dim, cudaStream_t stream,
+                            cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   if (a.g.n_items <= 0) return cudaSuccess;
-  if (head_dim == 128) return launch_fwd_d<128>(a, tq, tk, tv, stream);
-  return launch_fwd_d<64>(a, tq, tk, tv, stream);
+  if (head_dim == 128) return launch_fwd_d<128>(a, tq, tk, tv, stream, ev_start, ev_stop);
+  return launch_fwd_d<64>(a, tq, tk, tv, stream, ev_start, ev_stop);
 }
 
 }  // namespace mf

@@ -62,8 +62,10 @@ struct FwdArgs {
   float* lse;                // [heads, T]
 };
 
+// ev_start / ev_stop (may be null) are recorded around the main kernel.
 cudaError_t launch_attn_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, int head_dim, cudaStream_t stream);
+                            const CUtensorMap& tv, int head_dim, cudaStream_t stream,
+                            cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
 struct BwdArgs {
   AttnGeom g;
@@ -81,6 +83,6 @@ struct BwdArgs {
 
 cudaError_t launch_attn_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, int head_dim,
-                            cudaStream_t stream);
+                            cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
 }  // namespace mf
