@@ -161,6 +161,35 @@ MF_API mf_status mf_attn_bwd(const void *q, const void *k, const void *v, const 
                       int32_t head_dim, float softmax_scale, void *workspace,
                       size_t workspace_bytes, void *dq, void *dk, void *dv, void *stream);
 
+/* Size of the fixed device scratch behind mf_attn_bwd_noalloc (64 MiB). */
+#define MF_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* mf_attn_bwd for callers that cannot allocate device memory.  (The Mage-Flow
+ * pages have no counterpart: this is a deployment convenience of the
+ * library.)  Some callers cannot call cudaMalloc where they run the backward:
+ * an engine plugin whose execute step may not allocate, a runtime whose pool
+ * already owns all device memory, or a latency-critical loop that avoids
+ * cudaMalloc because it can synchronize the device.  This call takes the same
+ * arguments as mf_attn_bwd minus the workspace and uses instead a fixed
+ * MF_NOALLOC_SCRATCH_BYTES array of device memory that the library reserves
+ * on every GPU that loads it, held until the process exits.  It allocates
+ * nothing itself.
+ *   - The first call on a device looks up that array's device address (with
+ *     the device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Packs whose backward workspace (mf_attn_bwd_workspace_size) exceeds
+ *     MF_NOALLOC_SCRATCH_BYTES return MF_ERR_UNSUPPORTED without launching;
+ *     use mf_attn_bwd with a caller workspace for those.
+ *   - Every call on a device shares the one array.  Each call overwrites what
+ *     it needs before reading it, so earlier contents never leak into a
+ *     result, but calls that overlap on the GPU (e.g. on two streams at once)
+ *     race on the array and must be serialized by the caller.
+ * Other arguments, results and errors as mf_attn_bwd. */
+MF_API mf_status mf_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                                     const float *lse, const void *dout, const mf_plan *plan,
+                                     int32_t heads, int32_t head_dim, float softmax_scale,
+                                     void *dq, void *dk, void *dv, void *stream);
+
 /* Synchronize `stream`, then read and clear the plan's device status word:
  * MF_OK, MF_ERR_TIMEOUT, MF_ERR_RANGE, or MF_ERR_CUDA for a failed
  * synchronization. */

@@ -27,7 +27,8 @@ STATUS = {0: "MF_OK", 1: "MF_ERR_INVALID_ARG", 2: "MF_ERR_UNSUPPORTED", 3: "MF_E
           4: "MF_ERR_CUDA", 5: "MF_ERR_TIMEOUT", 6: "MF_ERR_RANGE"}
 
 EXPORTED_SYMBOLS = ["mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd",
-                    "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_record_main_kernel",
+                    "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_attn_bwd_noalloc", "mf_check",
+                    "mf_record_main_kernel",
                     "mf_status_string", "mf_last_cuda_error"]
 
 TILE = 128
