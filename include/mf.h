@@ -97,10 +97,12 @@ typedef struct {
   int32_t max_grid;     /* max_i max(H_i/16, W_i/16) */
   int32_t head_dim;     /* head_dim the RoPE table was built for */
   int32_t n_tiles;      /* sum_i ceil(L_i / MF_TILE) */
+  int32_t n_pairs;      /* sum_i ceil(L_i / (2 * MF_TILE)): forward work units */
   int32_t *cu_seqlens;  /* device int32 [n_samples + 1], exclusive scan of L_i */
   int32_t *pos;         /* device int32 [total_tokens][2]: (row, col); text = (-1, -1) */
   float *rope_cs;       /* device float32 [max_grid][head_dim/4][2]: cos, sin of p*f_i */
-  int32_t *order;       /* device int32 [n_samples][2]: (sample, first tile), longest sample first */
+  int32_t *order;       /* device int32 [n_samples][4]: (sample, first tile, first tile pair, 0),
+                           longest sample first */
   int32_t *status;      /* device int32 status word written by kernels that time out */
 } mf_plan;
 

@@ -42,6 +42,7 @@ class MfPlan(ctypes.Structure):
     _fields_ = [("n_samples", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
                 ("max_seqlen", ctypes.c_int32), ("max_grid", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
+                ("n_pairs", ctypes.c_int32),
                 ("cu_seqlens", ctypes.c_void_p), ("pos", ctypes.c_void_p),
                 ("rope_cs", ctypes.c_void_p), ("order", ctypes.c_void_p),
                 ("status", ctypes.c_void_p)]
@@ -126,6 +127,7 @@ class Plan:
     max_grid = property(lambda self: self.raw.max_grid)
     head_dim = property(lambda self: self.raw.head_dim)
     n_tiles = property(lambda self: self.raw.n_tiles)
+    n_pairs = property(lambda self: self.raw.n_pairs)
 
     @property
     def device(self):
@@ -147,7 +149,7 @@ class Plan:
         return self._view(self.raw.rope_cs, n, torch.float32).view(self.max_grid, self.head_dim // 4, 2)
 
     def order(self) -> torch.Tensor:
-        return self._view(self.raw.order, 2 * self.n_samples, torch.int32).view(-1, 2)
+        return self._view(self.raw.order, 4 * self.n_samples, torch.int32).view(-1, 4)
 
 
 def pack_plan(samples, token_budget: int = 0, head_dim: int = 128, rope_theta: float = 10000.0,

@@ -78,7 +78,7 @@ mf_status check_samples(const mf_sample* samples, int32_t n, int32_t budget, int
   L->off_cu = off;
   off = align_up(off + static_cast<size_t>(n + 1) * sizeof(int32_t), 256);
   L->off_order = off;
-  off = align_up(off + static_cast<size_t>(n) * 2 * sizeof(int32_t), 256);
+  off = align_up(off + static_cast<size_t>(n) * 4 * sizeof(int32_t), 256);
   L->off_pos = off;
   off = align_up(off + static_cast<size_t>(L->token_bound) * 2 * sizeof(int32_t), 256);
   L->off_rope = off;
@@ -141,6 +141,7 @@ mf_status check_attn_common(const mf_plan* plan, int32_t heads, int32_t head_dim
        plan->order == nullptr || plan->status == nullptr))
     return MF_ERR_INVALID_ARG;
   if (static_cast<long long>(plan->n_tiles) * heads >= (1ll << 31)) return MF_ERR_UNSUPPORTED;
+  if (plan->n_pairs < 0 || plan->n_pairs > plan->n_tiles) return MF_ERR_INVALID_ARG;
   return MF_OK;
 }
 
@@ -222,6 +223,7 @@ mf_status mf_pack_plan(const mf_sample* samples, int32_t n_samples, int32_t toke
   plan_out->max_grid = sc.max_grid;
   plan_out->head_dim = head_dim;
   plan_out->n_tiles = sc.n_tiles;
+  plan_out->n_pairs = sc.n_pairs;
   plan_out->cu_seqlens = a.cu_seqlens;
   plan_out->pos = a.pos;
   plan_out->rope_cs = a.rope_cs;
@@ -244,6 +246,7 @@ mf_status mf_attn_fwd(const void* q, const void* k, const void* v, const mf_plan
   if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   mf::FwdArgs a;
   a.g = make_geom(plan, heads);
+  a.g.n_items = plan->n_pairs * heads;  // the forward works on 256-row tile pairs
   a.scale_log2 = resolve_scale(softmax_scale, head_dim) * kLog2e;
   a.o = o;
   a.lse = lse;

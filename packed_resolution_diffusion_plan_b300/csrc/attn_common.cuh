@@ -16,20 +16,23 @@ struct WorkItem {
 };
 
 // Items are grouped per sample in longest-first order; inside a group the
-// head is the slow index and the tile the fast one, so CTAs that run at the
-// same time share one head's K/V (or Q/dO) in L2.
+// head is the slow index and the tile (kRows = 128) or tile pair (kRows =
+// 256) the fast one, so CTAs that run at the same time share one head's K/V
+// (or Q/dO) in L2.
+template <int kRows = kTile>
 __device__ __forceinline__ WorkItem decode_item(const AttnGeom& g, int item) {
+  constexpr int col = kRows == kTile ? 1 : 2;  // order column of the first unit
   int lo = 0, hi = g.n_samples;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (g.order[2 * mid + 1] * g.heads <= item) lo = mid; else hi = mid;
+    if (g.order[4 * mid + col] * g.heads <= item) lo = mid; else hi = mid;
   }
   WorkItem w;
-  w.sample = g.order[2 * lo];
-  const int start = g.order[2 * lo + 1];
+  w.sample = g.order[4 * lo];
+  const int start = g.order[4 * lo + col];
   w.seq_start = g.cu_seqlens[w.sample];
   w.len = g.cu_seqlens[w.sample + 1] - w.seq_start;
-  const int nt = (w.len + kTile - 1) / kTile;
+  const int nt = (w.len + kRows - 1) / kRows;
   const int local = item - start * g.heads;
   w.head = local / nt;
   w.tile = local - w.head * nt;

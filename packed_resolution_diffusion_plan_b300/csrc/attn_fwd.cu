@@ -6,24 +6,28 @@
 // tokens, confined to each sample by cumulative offsets; Hugging Face paper
 // page, Highlights "System-level speed": per-sample 2D RoPE).
 //
-// One CTA owns one 128-row Q tile of one (sample, head) and streams the
-// sample's 128-row K/V tiles:
-//   warp 4      TMA producer: Q once, then K/V tiles into a 2-stage ring
-//   warps 6-7   RoPE: rotate the Q tile and each landed K tile in shared
-//               memory (two rows per thread), so no rotated copy reaches HBM.
-//               The rotated rows are stored as fp16 (Q pre-multiplied by
-//               softmax_scale * log2 e): the logit MMA runs fp16 x fp16 ->
-//               fp32, whose 11-bit significand keeps the rounding of the
-//               rotated operands 8x below bf16's; S lands in TMEM already in
-//               exp2 units.  P V stays bf16 x bf16 (V is a bf16 input).
-//   warp 5      MMA issuer: S_j = Q K_j^T into TMEM (two S buffers), then
-//               O += P_j V_j into a TMEM accumulator
-//   warps 0-3   softmax: thread t owns query row t (TMEM lane t); online
-//               softmax in the exp2 domain, P_j written to shared memory as
-//               bf16, O rescaled in TMEM only when the running max grows by
-//               more than 2^8, epilogue O / l and LSE
-// Rows past the sample's end inside the last K/V tile are masked to -inf;
-// Q rows past the end are computed but never stored.
+// One CTA owns a pair of 128-row Q tiles (256 query rows) of one (sample,
+// head) and streams the sample's 128-row K/V tiles, so every K tile it
+// rotates serves 256 query rows.  16 warps in four warpgroups:
+//   WG0, WG1   softmax of Q tile 0 / 1: thread t owns query row t (TMEM lane
+//              t); online softmax in the exp2 domain, O rescaled in TMEM only
+//              when the running max grows by more than 2^8; P written back
+//              into its S columns of TMEM as packed bf16; epilogue O / l, LSE
+//   WG2        RoPE: rotates the Q tiles once and each landed K tile (one row
+//              per thread) in shared memory, so no rotated copy reaches HBM.
+//              Rotated rows are stored as fp16 (Q pre-multiplied by
+//              softmax_scale * log2 e): the logit MMA runs fp16 x fp16 -> fp32,
+//              whose 11-bit significand keeps the rotation's rounding 8x below
+//              bf16's, and S lands in TMEM already in exp2 units
+//   WG3        warp 12: TMA producer (Q pair once; K into a 3-slot ring freed
+//              right after both logit MMAs, V into a 2-slot ring); warp 13:
+//              TMEM owner and single-thread MMA issuer:
+//                S_a = Q_a K_j^T (smem x smem), O_a += P_a V_j (P from TMEM)
+// TMEM: S0 | S1 | O0 | O1 (128 + 128 + D + D columns of 512).  Registers are
+// rebalanced with setmaxnreg (the four warpgroup shares sum to the launch's
+// 4 x 128 per thread).
+// Rows past the sample's end: K/Q rows are zeroed after rotation, S columns
+// past the end are masked to -inf, Q rows past the end are never stored.
 #include "attn_common.cuh"
 
 namespace mf {
@@ -33,25 +37,50 @@ template <int D>
 struct FwdCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kPBytes = kTile * kTile * 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
-  static constexpr int kOffV = kOffK + 2 * kTileBytes;
-  static constexpr int kOffP = kOffV + 2 * kTileBytes;
-  static constexpr int kSmemBytes = kOffP + 2 * kPBytes;
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 2;
+  static constexpr int kOffQ = 0;                                 // Q0 | Q1
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kSmemBytes = kOffV + kVStages * kTileBytes;
   static constexpr int kDynSmem = kSmemBytes + 1024;
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;        // S_a at a * 128
+  static constexpr uint32_t kColO = 256;      // O_a at 256 + a * D
+  static constexpr uint32_t kTmemCols = 512;
 };
 
-// 8 warps = 2 per SM sub-partition, which leaves up to 255 registers per
-// thread for the softmax warps (128 fp32 logits live per thread).
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kRopeWarp0 = 6;
-constexpr int kRopeThreads = 64;
-constexpr int kThreads = 8 * 32;
+constexpr int kThreads = 16 * 32;
+constexpr int kRopeWG = 2;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
+// Per-thread register shares after setmaxnreg (chosen from ptxas spill
+// reports: the producer/MMA warpgroup needs ~80, RoPE ~72-80).
+constexpr uint32_t kRegsSoftmax = 176, kRegsRope = 80, kRegsCtrl = 80;
+static_assert(2 * kRegsSoftmax + kRegsRope + kRegsCtrl <= 4 * 128,
+              "warpgroup register shares exceed the launch's registers");
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]: A is M x 16 bf16 held as 8 TMEM columns of
+// packed pairs (lane = row, column c = elements 2c, 2c+1).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -60,30 +89,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_q_full, bar_q_rot, bar_final;
-  __shared__ uint64_t bar_k_full[2], bar_k_rot[2], bar_v_full[2], bar_kv_empty[2];
+  __shared__ uint64_t bar_q_full, bar_q_ready, bar_final;
+  __shared__ uint64_t bar_k_full[C::kKStages], bar_k_rot[C::kKStages], bar_k_free[C::kKStages];
+  __shared__ uint64_t bar_v_full[C::kVStages], bar_v_free[C::kVStages];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_range;
   __shared__ WorkItem s_item;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
   if (tid == 0) {
     mbar_init(&bar_q_full, 1);
-    mbar_init(&bar_q_rot, kRopeThreads);
+    mbar_init(&bar_q_ready, kTile);
     mbar_init(&bar_final, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&bar_k_full[i], 1);
-      mbar_init(&bar_k_rot[i], kRopeThreads);
+      mbar_init(&bar_k_rot[i], kTile);
+      mbar_init(&bar_k_free[i], 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
       mbar_init(&bar_v_full[i], 1);
-      mbar_init(&bar_kv_empty[i], 1);
+      mbar_init(&bar_v_free[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s_full[i], 1);
       mbar_init(&bar_p_full[i], kTile);
       mbar_init(&bar_pv_done[i], 1);
     }
     s_abort = 0;
     s_range = 0;
-    s_item = decode_item(args.g, blockIdx.x);
+    s_item = decode_item<2 * kTile>(args.g, blockIdx.x);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -95,131 +130,149 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   tc_fence_after();
 
   const uint32_t tmem = s_tmem;
-  const WorkItem w = s_item;
-  const int q0 = w.seq_start + w.tile * kTile;
-  const int q_rows = min(kTile, w.len - w.tile * kTile);
+  const WorkItem w = s_item;                   // w.tile = pair index
+  const int q0 = w.seq_start + w.tile * 2 * kTile;
+  const int rows_left = w.len - w.tile * 2 * kTile;
   const int n_kv = (w.len + kTile - 1) / kTile;
-  const int xcol = w.head * D;  // column of this head in the [T, heads*D] view
+  const int xcol = w.head * D;
 
-  if (warp == kProducerWarp) {
-    if (lane == 0) {
+  if (wg == 3) {
+    regs_dec<kRegsCtrl>();
+    if (warp == kProducerWarp && lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_arrive_expect_tx(&bar_q_full, C::kTileBytes);
-      for (int h = 0; h < C::kHalves; ++h)
-        tma_load_2d(smem + C::kOffQ + h * 16384, &tq, &bar_q_full, xcol + h * 64, q0);
-      int j = 0;
-      for (; j < n_kv; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&bar_kv_empty[s], ((j >> 1) - 1) & 1, &s_abort)) break;
-        const int y = w.seq_start + j * kTile;
-        mbar_arrive_expect_tx(&bar_k_full[s], C::kTileBytes);
+      mbar_arrive_expect_tx(&bar_q_full, 2 * C::kTileBytes);
+      for (int a = 0; a < 2; ++a)
         for (int h = 0; h < C::kHalves; ++h)
-          tma_load_2d(smem + C::kOffK + s * C::kTileBytes + h * 16384, &tk, &bar_k_full[s], xcol + h * 64, y);
-        mbar_arrive_expect_tx(&bar_v_full[s], C::kTileBytes);
-        for (int h = 0; h < C::kHalves; ++h)
-          tma_load_2d(smem + C::kOffV + s * C::kTileBytes + h * 16384, &tv, &bar_v_full[s], xcol + h * 64, y);
+          tma_load_2d(smem + C::kOffQ + a * C::kTileBytes + h * 16384, &tq, &bar_q_full, xcol + h * 64,
+                      q0 + a * kTile);
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      // K_j goes out one step ahead of V_j: the logit MMAs need it first.
+      for (int j = 0; ok && j <= n_kv; ++j) {
+        const int jk = j;  // K tile issued in this step
+        if (jk < n_kv) {
+          const int s = jk % C::kKStages;
+          if (jk >= C::kKStages && !mbar_wait(&bar_k_free[s], (jk / C::kKStages - 1) & 1, &s_abort)) break;
+          mbar_arrive_expect_tx(&bar_k_full[s], C::kTileBytes);
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_2d(smem + C::kOffK + s * C::kTileBytes + h * 16384, &tk, &bar_k_full[s], xcol + h * 64,
+                        w.seq_start + jk * kTile);
+          k_issued = jk + 1;
+        }
+        const int jv = j - 1;  // V tile issued in this step
+        if (jv >= 0) {
+          const int s = jv % C::kVStages;
+          if (jv >= C::kVStages && !mbar_wait(&bar_v_free[s], (jv / C::kVStages - 1) & 1, &s_abort)) break;
+          mbar_arrive_expect_tx(&bar_v_full[s], C::kTileBytes);
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_2d(smem + C::kOffV + s * C::kTileBytes + h * 16384, &tv, &bar_v_full[s], xcol + h * 64,
+                        w.seq_start + jv * kTile);
+          v_issued = jv + 1;
+        }
       }
       // Let this CTA's own copies land before its shared memory is released.
       wait_drain(&bar_q_full, 0);
-      for (int jj = max(0, j - 2); jj < j; ++jj) {
-        wait_drain(&bar_k_full[jj & 1], (jj >> 1) & 1);
-        wait_drain(&bar_v_full[jj & 1], (jj >> 1) & 1);
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {
+      for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
+        wait_drain(&bar_k_full[j % C::kKStages], (j / C::kKStages) & 1);
+      for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
+        wait_drain(&bar_v_full[j % C::kVStages], (j / C::kVStages) & 1);
+    } else if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(kTile, kTile, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(kTile, D, false, true);
       const uint32_t sQ = smem_u32(smem + C::kOffQ);
       const uint32_t sK = smem_u32(smem + C::kOffK);
       const uint32_t sV = smem_u32(smem + C::kOffV);
-      const uint32_t sP = smem_u32(smem + C::kOffP);
-      auto issue_pv = [&](int jj) -> bool {
-        const int bb = jj & 1;
-        if (!mbar_wait(&bar_p_full[bb], (jj >> 1) & 1, &s_abort)) return false;
-        if (!mbar_wait(&bar_v_full[bb], (jj >> 1) & 1, &s_abort)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t ad = smem_desc(sP + bb * C::kPBytes + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc(sV + bb * C::kTileBytes + kk * 2048, 16384, 1024);
-          mma_ss(tmem + C::kColO, ad, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bar_pv_done[bb]);
-        mma_commit(&bar_kv_empty[bb]);
-        return true;
-      };
-      bool ok = mbar_wait(&bar_q_rot, 0, &s_abort);
+      bool ok = mbar_wait(&bar_q_ready, 0, &s_abort);
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(&bar_k_rot[s], (j >> 1) & 1, &s_abort)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(&bar_p_full[s], ((j - 2) >> 1) & 1, &s_abort)) { ok = false; break; }
-        tc_fence_after();
+        const int sk = j % C::kKStages, sv = j % C::kVStages;
+        if (!mbar_wait(&bar_k_rot[sk], (j / C::kKStages) & 1, &s_abort)) { ok = false; break; }
+        for (int a = 0; a < 2 && ok; ++a) {
+          // S_a holds P_a(j-1) until PV_a(j-1) has read it.
+          if (j > 0 && !mbar_wait(&bar_pv_done[a], (j - 1) & 1, &s_abort)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + (s ? C::kColS1 : C::kColS0), smem_desc(sQ + off, 16, 1024),
-                 smem_desc(sK + s * C::kTileBytes + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tmem + C::kColS + a * kTile, smem_desc(sQ + a * C::kTileBytes + off, 16, 1024),
+                   smem_desc(sK + sk * C::kTileBytes + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar_s_full[a]);
         }
-        mma_commit(&bar_s_full[s]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        if (!ok) break;
+        mma_commit(&bar_k_free[sk]);
+        for (int a = 0; a < 2 && ok; ++a) {
+          if (!mbar_wait(&bar_p_full[a], j & 1, &s_abort)) { ok = false; break; }
+          if (a == 0 && !mbar_wait(&bar_v_full[sv], (j / C::kVStages) & 1, &s_abort)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            mma_ts(tmem + C::kColO + a * D, tmem + C::kColS + a * kTile + kk * 8,
+                   smem_desc(sV + sv * C::kTileBytes + kk * 2048, 16384, 1024), idesc_pv,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bar_pv_done[a]);
+        }
+        if (!ok) break;
+        mma_commit(&bar_v_free[sv]);
       }
-      if (ok) issue_pv(n_kv - 1);
       mma_commit(&bar_final);
       wait_drain(&bar_final, 0);
     }
-  } else if (warp >= kRopeWarp0) {
-    // Thread r prepares rows r and r + 64 of each tile for the logit MMA:
-    // fp16 of R(pos) q * scale * log2(e) for Q, fp16 of R(pos) k for K;
-    // rows past the sample's end are zeroed.
-    const int r = tid - kRopeWarp0 * 32;
+  } else if (wg == kRopeWG) {
+    regs_dec<kRegsRope>();
+    // Thread r prepares row r of each tile for the logit MMA: fp16 of
+    // R(pos) q * scale * log2(e) for Q, fp16 of R(pos) k for K; rows past the
+    // sample's end are zeroed.
+    const int r = tid - kRopeWG * 128;
     const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
     const float* tab = args.g.rope_cs;
     float amax = 0.f;
-    int2 pq0 = make_int2(-1, -1), pq1 = make_int2(-1, -1);
-    if (r < q_rows) pq0 = pos[q0 + r];
-    if (r + kRopeThreads < q_rows) pq1 = pos[q0 + r + kRopeThreads];
+    int2 pq[2];
+#pragma unroll
+    for (int a = 0; a < 2; ++a) pq[a] = (a * kTile + r < rows_left) ? pos[q0 + a * kTile + r] : make_int2(-1, -1);
     if (mbar_wait(&bar_q_full, 0, &s_abort)) {
-      uint8_t* qt = smem + C::kOffQ;
-      if (r < q_rows) amax = fmaxf(amax, rope_row_to_f16<D>(qt, r, pq0, tab, args.scale_log2));
-      else zero_row<D>(qt, r);
-      if (r + kRopeThreads < q_rows) amax = fmaxf(amax, rope_row_to_f16<D>(qt, r + kRopeThreads, pq1, tab, args.scale_log2));
-      else zero_row<D>(qt, r + kRopeThreads);
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        uint8_t* qt = smem + C::kOffQ + a * C::kTileBytes;
+        if (a * kTile + r < rows_left) amax = fmaxf(amax, rope_row_to_f16<D>(qt, r, pq[a], tab, args.scale_log2));
+        else zero_row<D>(qt, r);
+      }
       fence_proxy_async_smem();
-      mbar_arrive(&bar_q_rot);
+      mbar_arrive(&bar_q_ready);
+      int2 pk = (r < w.len) ? pos[w.seq_start + r] : make_int2(-1, -1);
       for (int j = 0; j < n_kv; ++j) {
-        const int s = j & 1;
+        const int s = j % C::kKStages;
         const int kr = j * kTile + r;
-        int2 pk0 = make_int2(-1, -1), pk1 = make_int2(-1, -1);
-        if (kr < w.len) pk0 = pos[w.seq_start + kr];
-        if (kr + kRopeThreads < w.len) pk1 = pos[w.seq_start + kr + kRopeThreads];
-        if (!mbar_wait(&bar_k_full[s], (j >> 1) & 1, &s_abort)) break;
+        // next tile's position, loaded while this one is in flight
+        const int2 pk_next = (kr + kTile < w.len) ? pos[w.seq_start + kr + kTile] : make_int2(-1, -1);
+        if (!mbar_wait(&bar_k_full[s], (j / C::kKStages) & 1, &s_abort)) break;
         uint8_t* kt = smem + C::kOffK + s * C::kTileBytes;
-        if (kr < w.len) amax = fmaxf(amax, rope_row_to_f16<D>(kt, r, pk0, tab, 1.0f));
+        if (kr < w.len) amax = fmaxf(amax, rope_row_to_f16<D>(kt, r, pk, tab, 1.0f));
         else zero_row<D>(kt, r);
-        if (kr + kRopeThreads < w.len) amax = fmaxf(amax, rope_row_to_f16<D>(kt, r + kRopeThreads, pk1, tab, 1.0f));
-        else zero_row<D>(kt, r + kRopeThreads);
         fence_proxy_async_smem();
         mbar_arrive(&bar_k_rot[s]);
+        pk = pk_next;
       }
     }
     if (!(amax <= kF16Max)) s_range = 1;
   } else {
-    // Softmax warpgroup: thread `tid` owns query row `tid`.
-    const int row = tid;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    regs_inc<kRegsSoftmax>();
+    // Softmax warpgroup `a`: thread `row` owns query row `row` of Q tile a.
+    const int a = wg;
+    const int row = tid & (kTile - 1);
+    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t colS = C::kColS + a * kTile, colO = C::kColO + a * D;
     const int last_valid = w.len - (n_kv - 1) * kTile;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      if (!warp_wait(&bar_s_full[b], (j >> 1) & 1, &s_abort)) { ok = false; break; }
+      if (!warp_wait(&bar_s_full[a], j & 1, &s_abort)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tl + (b ? C::kColS1 : C::kColS0) + c * 32, sr[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(tl + colS + c * 32, sr[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
       if (j == n_kv - 1 && last_valid < kTile) {
@@ -235,63 +288,62 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
         for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
       const float m_new = fmaxf(m_run, mx);
-      // P buffer b is free once PV_{j-2} has completed.
-      if (j >= 2 && !warp_wait(&bar_pv_done[b], ((j - 2) >> 1) & 1, &s_abort)) { ok = false; break; }
       const bool need = m_new > m_run + kRescaleThreshold;
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        if (!warp_wait(&bar_pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, &s_abort)) { ok = false; break; }
-        tc_fence_after();
-        const float f = need ? ex2_approx(m_run - m_new) : 1.f;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tl + C::kColO + c * 32, o);
-          tmem_wait_ld(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-          tmem_st32(tl + C::kColO + c * 32, o);
-        }
-        tmem_wait_st();
-      }
+      const bool rescale_o = j > 0 && __any_sync(0xffffffffu, need);
+      float alpha = 1.f;
       if (need) {
-        l_run *= ex2_approx(m_run - m_new);
+        alpha = ex2_approx(m_run - m_new);
+        l_run *= alpha;
         m_run = m_new;
       }
       const float neg_m = -m_run;
       float rs = 0.f;
-      uint8_t* Pb = smem + C::kOffP + b * C::kPBytes;
+      // P as packed bf16 pairs over S's first 64 columns (all of S is in
+      // registers already), 16 columns at a time so the logits die early.
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        uint32_t pw[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float p[8];
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(__uint_as_float(sr[c][2 * i]) + neg_m);
+          const float p1 = ex2_approx(__uint_as_float(sr[c][2 * i + 1]) + neg_m);
+          rs += p0 + p1;
+          pw[i] = pack_bf16(p0, p1);
+        }
+        tmem_st16(tl + colS + c * 16, pw);
+      }
+      if (rescale_o) {
+        // O_a is stable once PV_a(j-1) has completed; PV_a(j) is not issued
+        // before p_full below.
+        if (!warp_wait(&bar_pv_done[a], (j - 1) & 1, &s_abort)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            p[e] = ex2_approx(__uint_as_float(sr[c][q * 8 + e]) + neg_m);
-            rs += p[e];
-          }
-          const int ch = c * 4 + q;  // 16-byte chunk 0..15 of the 256-byte P row
-          uint4 v = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
-                               pack_bf16(p[6], p[7]));
-          *reinterpret_cast<uint4*>(Pb + (ch >> 3) * 16384 + sw128_off(row, ch & 7)) = v;
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tl + colO + c * 32, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tl + colO + c * 32, o);
         }
       }
+      tmem_wait_st();
       l_run += rs;
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar_p_full[b]);
+      mbar_arrive(&bar_p_full[a]);
     }
-    if (ok) ok = warp_wait(&bar_pv_done[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, &s_abort);
+    if (ok) ok = warp_wait(&bar_pv_done[a], (n_kv - 1) & 1, &s_abort);
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l_run;
-      const bool valid = row < q_rows;
+      const int qrow = a * kTile + row;
+      const bool valid = qrow < rows_left;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) +
-                            (static_cast<size_t>(q0 + row) * args.g.heads + w.head) * D;
+                            (static_cast<size_t>(q0 + qrow) * args.g.heads + w.head) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tl + C::kColO + c * 32, o);
+        tmem_ld32(tl + colO + c * 32, o);
         tmem_wait_ld(o);
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
@@ -305,7 +357,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
       }
       if (valid)
-        args.lse[static_cast<size_t>(w.head) * args.g.total_tokens + q0 + row] = (m_run + __log2f(l_run)) * kLn2;
+        args.lse[static_cast<size_t>(w.head) * args.g.total_tokens + q0 + qrow] = (m_run + __log2f(l_run)) * kLn2;
     }
   }
 

@@ -20,7 +20,8 @@ struct PlanScalars {
   int32_t max_grid;
   int32_t n_tiles;
   int32_t status;
-  int32_t pad[2];
+  int32_t n_pairs;
+  int32_t pad;
 };
 
 struct PlanArgs {
@@ -29,7 +30,7 @@ struct PlanArgs {
   int32_t budget;           // 0 = none
   PlanScalars* scalars;
   int32_t* cu_seqlens;      // [n+1]
-  int32_t* order;           // [n][2]
+  int32_t* order;           // [n][4]
   int32_t* pos;             // [token_bound][2]
   int32_t token_bound;
   float* rope_cs;           // [grid_bound][head_dim/4][2]
@@ -41,8 +42,9 @@ struct PlanArgs {
 cudaError_t launch_pack_plan(const PlanArgs& a, cudaStream_t stream);
 
 // Attention work decode: the plan's order list holds, per sample sorted by
-// length (longest first), the sample index and its first tile index in that
-// order; a CTA item is (sorted sample, head, tile) with tiles fastest.
+// length (longest first), the sample index, its first 128-row tile index and
+// its first 256-row tile-pair index in that order; a CTA item is (sorted
+// sample, head, tile or pair) with the tile / pair fastest.
 struct AttnGeom {
   const int32_t* cu_seqlens;
   const int32_t* pos;
@@ -51,7 +53,7 @@ struct AttnGeom {
   int32_t n_samples;
   int32_t total_tokens;
   int32_t heads;
-  int32_t n_items;          // n_tiles * heads
+  int32_t n_items;          // work units (tiles or pairs) * heads
   int32_t* status;
 };
 

@@ -97,26 +97,35 @@ __global__ void __launch_bounds__(kPlanThreads) pack_scan_kernel(PlanArgs a) {
     s_sorted[rank] = i;
   }
   __syncthreads();
-  long long nt_local = 0;
-  long long nt_mine[kPerThread];
+  long long nt_local = 0, np_local = 0;
+  long long nt_mine[kPerThread], np_mine[kPerThread];
 #pragma unroll
   for (int u = 0; u < kPerThread; ++u) {
     const int r = t * kPerThread + u;
-    long long nt = 0;
-    if (r < np) nt = (s_len[s_sorted[r]] + kTile - 1) / kTile;
+    long long nt = 0, npair = 0;
+    if (r < np) {
+      nt = (s_len[s_sorted[r]] + kTile - 1) / kTile;
+      npair = (s_len[s_sorted[r]] + 2 * kTile - 1) / (2 * kTile);
+    }
     nt_mine[u] = nt;
+    np_mine[u] = npair;
     nt_local += nt;
+    np_local += npair;
   }
-  long long n_tiles;
+  long long n_tiles, n_pairs;
   long long start = block_exclusive_scan(nt_local, s_warp, &n_tiles);
+  long long pstart = block_exclusive_scan(np_local, s_warp, &n_pairs);
 #pragma unroll
   for (int u = 0; u < kPerThread; ++u) {
     const int r = t * kPerThread + u;
     if (r < np) {
-      a.order[2 * r] = s_sorted[r];
-      a.order[2 * r + 1] = static_cast<int32_t>(start);
+      a.order[4 * r] = s_sorted[r];
+      a.order[4 * r + 1] = static_cast<int32_t>(start);
+      a.order[4 * r + 2] = static_cast<int32_t>(pstart);
+      a.order[4 * r + 3] = 0;
     }
     start += nt_mine[u];
+    pstart += np_mine[u];
   }
   if (t == 0) {
     long long total = 0;
@@ -127,6 +136,7 @@ __global__ void __launch_bounds__(kPlanThreads) pack_scan_kernel(PlanArgs a) {
     a.scalars->max_seqlen = s_maxlen;
     a.scalars->max_grid = s_maxgrid;
     a.scalars->n_tiles = static_cast<int32_t>(n_tiles);
+    a.scalars->n_pairs = static_cast<int32_t>(n_pairs);
     a.scalars->status = 0;
   }
 }

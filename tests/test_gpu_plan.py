@@ -29,8 +29,12 @@ def _check_plan(samples, budget, head_dim=128, theta=10000.0):
     want = sorted(range(len(lens)), key=lambda i: (-lens[i], i))
     assert list(order[:, 0]) == want
     tiles = [math.ceil(lens[i] / 128) for i in want]
-    assert list(order[:, 1]) == list(np.concatenate([[0], np.cumsum(tiles)[:-1]]).astype(int)) if want else True
-    assert p.n_tiles == sum(tiles)
+    pairs = [math.ceil(lens[i] / 256) for i in want]
+    if want:
+        assert list(order[:, 1]) == list(np.concatenate([[0], np.cumsum(tiles)[:-1]]).astype(int))
+        assert list(order[:, 2]) == list(np.concatenate([[0], np.cumsum(pairs)[:-1]]).astype(int))
+        assert list(order[:, 3]) == [0] * len(want)
+    assert p.n_tiles == sum(tiles) and p.n_pairs == sum(pairs)
     # RoPE table: cos/sin of p * theta^(-2i/(D/2)) rounded once to float32
     if p.max_grid:
         tab = p.rope_table().cpu().numpy().astype(np.float64)
