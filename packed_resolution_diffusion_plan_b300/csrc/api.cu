@@ -318,6 +318,10 @@ mf_status mf_check(const mf_plan* plan, void* stream) {
     e = cudaMemsetAsync(plan->status, 0, sizeof(int32_t), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "mf_check: clear status");
+    if (status & mf::kStatusLayout) {
+      g_last_cuda_error = "a kernel found its shared memory misaligned and did no work";
+      return MF_ERR_CUDA;
+    }
     return (status & mf::kStatusTimeout) ? MF_ERR_TIMEOUT : MF_ERR_RANGE;
   }
   return MF_OK;

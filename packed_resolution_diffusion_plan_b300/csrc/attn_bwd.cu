@@ -10,49 +10,83 @@
 // Three kernels:
 //   bwd_pre      D = rowsum(dO * O) (float32 [heads, T]); zero the float32 dQ
 //                accumulator.
-//   bwd_main     one CTA per (sample, head, 128-row K/V tile); loops over the
-//                sample's 128-row Q tiles with five tcgen05 MMAs per step:
-//                  S^T  = k~ q~^T            (fp16 x fp16, TMEM cols 0..127)
-//                  dP^T = V dO^T             (bf16 x bf16, TMEM cols 128..255)
-//                  dV  += P^T dO             (bf16, TMEM, accumulated over Q tiles)
-//                  dk~ += dS^T q~            (fp16, TMEM, accumulated)
-//                  dQ   = dS k~              (fp16, reuses cols 0..D-1 of S^T)
-//                P^T (bf16) and dS^T (fp16) are formed by the compute warps
-//                in shared memory; dQ is added to the accumulator with vector
-//                atomics; the epilogue writes dV and R^T dk~.
+//   bwd_main     one CTA per (sample, head, 128-row K/V tile), streaming the
+//                sample's 128-row Q/dO tiles through two-slot rings.  Per Q
+//                tile i, five tcgen05 MMAs (TMEM columns: A = 0..127,
+//                B = 128..255, dV = 256.., dK = 256 + D..):
+//                  S^T_i  = k~ q~_i^T        fp16, smem x smem -> A
+//                  dP^T_i = V dO_i^T         bf16, smem x smem -> B
+//                  dV    += P^T_i dO_i       bf16, P^T from TMEM (A) x smem
+//                  dk~   += dS^T_i q~_i      fp16, smem x smem
+//                  dQ_i   = dS_i k~          fp16, smem x smem -> B; with
+//                           head_dim 128 it is formed transposed (k~^T dS^T,
+//                           TMEM lane = dimension) so that a warp's float
+//                           atomics into the accumulator cover one 128-byte
+//                           line per query row
+//                issued in the order dV_i, dK_i, S^T_{i+1}, dQ_i, dP^T_{i+1},
+//                so the exponentials of tile i+1 overlap dQ_i and dP^T_{i+1}.
+//                16 warps:
+//                  WG0, WG1  thread r owns K/V row r (TMEM lane r), WG c the
+//                            query columns 64c..64c+63: P^T = exp2(S^T - LSE2)
+//                            written back over its S^T columns as packed bf16,
+//                            dS^T = P^T * (dP^T - D) as fp16 into shared
+//                            memory; at the end dV and R^T dk~ to HBM
+//                  WG2       RoPE of the K tile (once) and of every Q tile
+//                            (fp16, Q pre-scaled by s * log2 e so S^T is in
+//                            exp2 units), per-tile LSE2 / D rows into shared
+//                            memory; the dQ epilogue (TMEM -> float atomics)
+//                  WG3       warp 12 TMA producer, warp 13 TMEM owner and MMA
+//                            issuer
 //   bwd_dq       dq = R^T (s * accumulator) as bf16.
-// As in the forward, the rotated Q/K rows are fp16 (Q pre-scaled by
-// s * log2 e) so S^T comes out in exp2 units.
 #include "attn_common.cuh"
 
 namespace mf {
 namespace {
 
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kRopeWarp0 = 6;
-constexpr int kRopeThreads = 64;
-constexpr int kComputeThreads = 128;
-constexpr int kThreads = 8 * 32;
+constexpr int kThreads = 16 * 32;
+constexpr int kRopeWG = 2;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
+// Per-thread register shares after setmaxnreg; they add up to the launch's
+// 4 x 128 per thread.
+constexpr uint32_t kRegsCompute = 176, kRegsRope = 88, kRegsCtrl = 72;
+constexpr int kRopeUnroll = 4;
+static_assert(2 * kRegsCompute + kRegsRope + kRegsCtrl <= 4 * 128,
+              "warpgroup register shares exceed the launch's registers");
+
+// Barriers and CTA-wide scalars of bwd_main, kept in dynamic shared memory
+// after the tiles (the kernel has no static shared memory, so the dynamic
+// base is the start of the CTA's window and the tiles stay 1024-aligned).
+struct BwdCtl {
+  uint64_t kv_full, k_ready, fin;
+  uint64_t q_full[2], q_ready[2], q_free[2], do_full[2], do_free[2];
+  uint64_t s_full, p_ready, dp_full, ds_ready, dv_done, dq_full, dq_free;
+  uint32_t tmem;
+  int abort;
+  int range;
+  int pad;
+  WorkItem item;
+};
 
 template <int D>
 struct BwdCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kSqBytes = kTile * kTile * 2;  // P^T / dS^T tile
+  static constexpr int kSqBytes = kTile * kTile * 2;     // dS^T tile (fp16)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffQ = kOffV + kTileBytes;
-  static constexpr int kOffDO = kOffQ + kTileBytes;
-  static constexpr int kOffP = kOffDO + kTileBytes;
-  static constexpr int kOffDS = kOffP + kSqBytes;
-  static constexpr int kOffRow = kOffDS + kSqBytes;      // [2][2][128] float: lse2, D
-  static constexpr int kSmemBytes = kOffRow + 2 * 2 * kTile * 4;
-  static constexpr int kDynSmem = kSmemBytes + 1024;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 0;
+  static constexpr int kOffQ = kOffV + kTileBytes;       // 2 slots
+  static constexpr int kOffDO = kOffQ + 2 * kTileBytes;  // 2 slots
+  static constexpr int kOffDS = kOffDO + 2 * kTileBytes;
+  static constexpr int kOffRow = kOffDS + kSqBytes;      // [2 slots][LSE2[128] | D[128]] float
+  static constexpr int kOffCtl = kOffRow + 2 * 2 * kTile * 4;
+  static constexpr int kDynSmem = kOffCtl + 256;
+  static constexpr uint32_t kColA = 0, kColB = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr uint32_t kTmemCols = 512;
+  static_assert(sizeof(BwdCtl) <= 256, "control block");
+  static_assert(kDynSmem <= 232448, "shared memory");
 };
 
 // ---------------------------------------------------------------- bwd_pre
@@ -163,269 +197,375 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                 const BwdArgs args) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_kv_full, bar_k_ready, bar_q_full, bar_q_ready, bar_do_full;
-  __shared__ uint64_t bar_st_full, bar_ds_ready, bar_dv_done, bar_dk_done, bar_dq_full, bar_dq_free, bar_final;
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_abort, s_range;
-  __shared__ WorkItem s_item;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // The swizzled tiles need a 1024-byte aligned base; every thread sees the
+  // same address, so a misaligned window makes the whole CTA leave at once.
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(args.g.status, kStatusLayout);
+    return;
+  }
+  BwdCtl& c = *reinterpret_cast<BwdCtl*>(smem + C::kOffCtl);
+  float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow);
+  volatile int* abort_flag = &c.abort;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
   if (tid == 0) {
-    mbar_init(&bar_kv_full, 1);
-    mbar_init(&bar_k_ready, kRopeThreads);
-    mbar_init(&bar_q_full, 1);
-    mbar_init(&bar_q_ready, kRopeThreads);
-    mbar_init(&bar_do_full, 1);
-    mbar_init(&bar_st_full, 1);
-    mbar_init(&bar_ds_ready, kComputeThreads);
-    mbar_init(&bar_dv_done, 1);
-    mbar_init(&bar_dk_done, 1);
-    mbar_init(&bar_dq_full, 1);
-    mbar_init(&bar_dq_free, kComputeThreads);
-    mbar_init(&bar_final, 1);
-    s_abort = 0;
-    s_range = 0;
-    s_item = decode_item(args.g, blockIdx.x);
+    mbar_init(&c.kv_full, 1);
+    mbar_init(&c.k_ready, kTile);
+    mbar_init(&c.fin, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&c.q_full[s], 1);
+      mbar_init(&c.q_ready[s], kTile);
+      mbar_init(&c.q_free[s], 1);
+      mbar_init(&c.do_full[s], 1);
+      mbar_init(&c.do_free[s], 1);
+    }
+    mbar_init(&c.s_full, 1);
+    mbar_init(&c.p_ready, 2 * kTile);
+    mbar_init(&c.dp_full, 1);
+    mbar_init(&c.ds_ready, 2 * kTile);
+    mbar_init(&c.dv_done, 1);
+    mbar_init(&c.dq_full, 1);
+    mbar_init(&c.dq_free, kTile);
+    c.abort = 0;
+    c.range = 0;
+    c.item = decode_item(args.g, blockIdx.x);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(&s_tmem, C::kTmemCols);
+    tmem_alloc(&c.tmem, C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  const uint32_t tmem = s_tmem;
-  const WorkItem w = s_item;             // w.tile = this CTA's K/V tile
+  const uint32_t tmem = c.tmem;
+  const WorkItem w = c.item;             // w.tile = this CTA's K/V tile
   const int kv0 = w.seq_start + w.tile * kTile;
   const int kv_rows = min(kTile, w.len - w.tile * kTile);
   const int n_q = (w.len + kTile - 1) / kTile;
   const int xcol = w.head * D;
   const int T = args.g.total_tokens;
 
-  if (warp == kProducerWarp) {
-    if (lane == 0) {
+  if (wg == 3) {
+    regs_dec<kRegsCtrl>();
+    if (warp == kProducerWarp && lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
       tma_prefetch_desc(&tdo);
-      mbar_arrive_expect_tx(&bar_kv_full, 2 * C::kTileBytes);
+      mbar_arrive_expect_tx(&c.kv_full, 2 * C::kTileBytes);
       for (int h = 0; h < C::kHalves; ++h) {
-        tma_load_2d(smem + C::kOffK + h * 16384, &tk, &bar_kv_full, xcol + h * 64, kv0);
-        tma_load_2d(smem + C::kOffV + h * 16384, &tv, &bar_kv_full, xcol + h * 64, kv0);
+        tma_load_2d(smem + C::kOffK + h * 16384, &tk, &c.kv_full, xcol + h * 64, kv0);
+        tma_load_2d(smem + C::kOffV + h * 16384, &tv, &c.kv_full, xcol + h * 64, kv0);
       }
-      int i = 0, issued_do = 0, issued_q = 0;
-      for (; i < n_q; ++i) {
+      int nq_issued = 0, ndo_issued = 0;
+      for (int i = 0; i < n_q; ++i) {
+        const int s = i & 1;
+        const uint32_t ph_free = ((i >> 1) - 1) & 1;  // completion i/2 - 1 of the slot's free barrier
         const int y = w.seq_start + i * kTile;
-        if (i > 0 && !mbar_wait(&bar_dv_done, (i - 1) & 1, &s_abort)) break;
-        mbar_arrive_expect_tx(&bar_do_full, C::kTileBytes);
+        if (i >= 2 && !mbar_wait(&c.q_free[s], ph_free, abort_flag)) break;
+        mbar_arrive_expect_tx(&c.q_full[s], C::kTileBytes);
         for (int h = 0; h < C::kHalves; ++h)
-          tma_load_2d(smem + C::kOffDO + h * 16384, &tdo, &bar_do_full, xcol + h * 64, y);
-        issued_do = i + 1;
-        if (i > 0 && !mbar_wait(&bar_dk_done, (i - 1) & 1, &s_abort)) break;
-        mbar_arrive_expect_tx(&bar_q_full, C::kTileBytes);
+          tma_load_2d(smem + C::kOffQ + s * C::kTileBytes + h * 16384, &tq, &c.q_full[s], xcol + h * 64, y);
+        nq_issued = i + 1;
+        if (i >= 2 && !mbar_wait(&c.do_free[s], ph_free, abort_flag)) break;
+        mbar_arrive_expect_tx(&c.do_full[s], C::kTileBytes);
         for (int h = 0; h < C::kHalves; ++h)
-          tma_load_2d(smem + C::kOffQ + h * 16384, &tq, &bar_q_full, xcol + h * 64, y);
-        issued_q = i + 1;
+          tma_load_2d(smem + C::kOffDO + s * C::kTileBytes + h * 16384, &tdo, &c.do_full[s], xcol + h * 64, y);
+        ndo_issued = i + 1;
       }
-      wait_drain(&bar_kv_full, 0);
-      if (issued_do) wait_drain(&bar_do_full, (issued_do - 1) & 1);
-      if (issued_q) wait_drain(&bar_q_full, (issued_q - 1) & 1);
-    }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {
+      // Let this CTA's own copies land before its shared memory is released.
+      wait_drain(&c.kv_full, 0);
+      for (int j = max(0, nq_issued - 2); j < nq_issued; ++j) wait_drain(&c.q_full[j & 1], (j >> 1) & 1);
+      for (int j = max(0, ndo_issued - 2); j < ndo_issued; ++j) wait_drain(&c.do_full[j & 1], (j >> 1) & 1);
+    } else if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t id_st = idesc_f16(kTile, kTile, false, false);   // k~ q~^T
       constexpr uint32_t id_dp = idesc_bf16(kTile, kTile, false, false);  // V dO^T
       constexpr uint32_t id_dv = idesc_bf16(kTile, D, false, true);       // P^T dO
       constexpr uint32_t id_dk = idesc_f16(kTile, D, false, true);        // dS^T q~
-      constexpr uint32_t id_dq = idesc_f16(kTile, D, true, true);         // dS k~
+      // dQ: head_dim 128 forms dQ^T = k~^T dS^T (M = dimension); head_dim 64
+      // forms dQ = dS k~ (M = query row).
+      constexpr uint32_t id_dq = D == 128 ? idesc_f16(D, kTile, true, true) : idesc_f16(kTile, D, true, true);
       const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
       const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
-      const uint32_t sP = smem_u32(smem + C::kOffP), sDS = smem_u32(smem + C::kOffDS);
-      bool ok = mbar_wait(&bar_k_ready, 0, &s_abort) && mbar_wait(&bar_kv_full, 0, &s_abort);
-      for (int i = 0; ok && i < n_q; ++i) {
-        const uint32_t ph = i & 1;
-        if (!mbar_wait(&bar_q_ready, ph, &s_abort) || !mbar_wait(&bar_do_full, ph, &s_abort) ||
-            (i > 0 && !mbar_wait(&bar_dq_free, (i - 1) & 1, &s_abort))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
+      const uint32_t sDS = smem_u32(smem + C::kOffDS);
+      // K-major operands: 16-byte leading, 1024-byte stride; MN-major ones:
+      // two 64-element halves 16 KB apart.
+      auto kmaj = [](uint32_t a) { return sdesc<16, 1024>(a); };
+      auto mnmaj = [](uint32_t a) { return sdesc<16384, 1024>(a); };
+      auto issue_s = [&](int s) {
+#pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kColS, smem_desc(sK + off, 16, 1024), smem_desc(sQ + off, 16, 1024), id_st, kk > 0);
+          mma_ss(tmem + C::kColA, kmaj(sK + off), kmaj(sQ + s * C::kTileBytes + off),
+                 id_st, kk > 0 ? 1u : 0u);
         }
-#pragma unroll
+      };
+      auto issue_dp = [&](int s) {
+#pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDP, smem_desc(sV + off, 16, 1024), smem_desc(sDO + off, 16, 1024), id_dp, kk > 0);
+          mma_ss(tmem + C::kColB, kmaj(sV + off), kmaj(sDO + s * C::kTileBytes + off),
+                 id_dp, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar_st_full);
-        if (!mbar_wait(&bar_ds_ready, ph, &s_abort)) { ok = false; break; }
+      };
+      bool ok = mbar_wait(&c.k_ready, 0, abort_flag) && mbar_wait(&c.kv_full, 0, abort_flag) &&
+                mbar_wait(&c.q_ready[0], 0, abort_flag);
+      if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDV, smem_desc(sP + off, 16, 1024), smem_desc(sDO + kk * 2048, 16384, 1024), id_dv,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bar_dv_done);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDK, smem_desc(sDS + off, 16, 1024), smem_desc(sQ + kk * 2048, 16384, 1024), id_dk,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bar_dk_done);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          mma_ss(tmem + C::kColDQ, smem_desc(sDS + kk * 2048, 16384, 1024), smem_desc(sK + kk * 2048, 16384, 1024),
-                 id_dq, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar_dq_full);
+        issue_s(0);
+        mma_commit(&c.s_full);
+        ok = mbar_wait(&c.do_full[0], 0, abort_flag);
       }
-      mma_commit(&bar_final);
-      wait_drain(&bar_final, 0);
+      if (ok) {
+        tc_fence_after();
+        issue_dp(0);
+        mma_commit(&c.dp_full);
+      }
+      for (int i = 0; ok && i < n_q; ++i) {
+        const int s = i & 1, s1 = (i + 1) & 1;
+        const uint32_t ph = i & 1, ph1 = ((i + 1) >> 1) & 1;
+        const bool more = i + 1 < n_q;
+        // dV += P^T_i dO_i, with P^T packed in the A columns each compute
+        // warpgroup read its S^T from (query 64c.. at column 64c).
+        if (!mbar_wait(&c.p_ready, ph, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + C::kColDV, tmem + C::kColA + 64 * (kk >> 2) + 8 * (kk & 3),
+                 mnmaj(sDO + s * C::kTileBytes + kk * 2048), id_dv, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&c.dv_done);
+        mma_commit(&c.do_free[s]);
+        // dk~ += dS^T_i q~_i
+        if (!mbar_wait(&c.ds_ready, ph, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + C::kColDK, kmaj(sDS + off), mnmaj(sQ + s * C::kTileBytes + kk * 2048), id_dk, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&c.q_free[s]);
+        // S^T_{i+1} into A once dV_i has read P^T_i out of it.
+        if (more) {
+          if (!mbar_wait(&c.q_ready[s1], ph1, abort_flag) || !mbar_wait(&c.dv_done, ph, abort_flag)) break;
+          tc_fence_after();
+          issue_s(s1);
+          mma_commit(&c.s_full);
+        }
+        // dQ_i into B (the compute warps have read dP^T_i before ds_ready).
+#pragma unroll 1
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          if (D == 128)
+            mma_ss(tmem + C::kColB, mnmaj(sK + kk * 2048), mnmaj(sDS + kk * 2048),
+                   id_dq, kk > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + C::kColB, mnmaj(sDS + kk * 2048), mnmaj(sK + kk * 2048),
+                   id_dq, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&c.dq_full);
+        // dP^T_{i+1} into B once the epilogue has read dQ_i out of it.
+        if (more) {
+          if (!mbar_wait(&c.do_full[s1], ph1, abort_flag) || !mbar_wait(&c.dq_free, ph, abort_flag)) break;
+          tc_fence_after();
+          issue_dp(s1);
+          mma_commit(&c.dp_full);
+        }
+      }
+      mma_commit(&c.fin);
+      wait_drain(&c.fin, 0);
     }
-  } else if (warp >= kRopeWarp0) {
-    // fp16 k~ (once) and fp16 q~ * s * log2 e (per Q tile); rows past the
-    // sample's end are zeroed.
-    const int r = tid - kRopeWarp0 * 32;
+  } else if (wg == kRopeWG) {
+    regs_dec<kRegsRope>();
+    const int r = tid - kRopeWG * 128;
     const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
     const float* tab = args.g.rope_cs;
+    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     float amax = 0.f;
-    if (mbar_wait(&bar_kv_full, 0, &s_abort)) {
-      uint8_t* kt = smem + C::kOffK;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int rr = r + u * kRopeThreads;
-        if (rr < kv_rows) amax = fmaxf(amax, rope_row_to_f16<D>(kt, rr, pos[kv0 + rr], tab, 1.0f));
-        else zero_row<D>(kt, rr);
-      }
+    // fp16 q~ * s * log2 e of row r of Q tile i, and that row's LSE2 / D.
+    auto rope_q = [&](int i) -> bool {
+      const int s = i & 1;
+      const int q0 = w.seq_start + i * kTile;
+      const bool valid = r < w.len - i * kTile;
+      const size_t idx = static_cast<size_t>(w.head) * T + q0 + r;
+      const int2 p = valid ? pos[q0 + r] : make_int2(-1, -1);
+      const float l2 = valid ? args.lse[idx] * kLog2e : INFINITY;  // invalid query: P = 0
+      const float dd = valid ? args.dsum[idx] : 0.f;
+      if (!warp_wait(&c.q_full[s], (i >> 1) & 1, abort_flag)) return false;
+      uint8_t* qt = smem + C::kOffQ + s * C::kTileBytes;
+      if (valid) amax = fmaxf(amax, rope_row_to_f16<D, kRopeUnroll>(qt, r, p, tab, args.scale_log2));
+      else zero_row<D>(qt, r);
+      rowbuf[s * 2 * kTile + r] = l2;
+      rowbuf[s * 2 * kTile + kTile + r] = dd;
       fence_proxy_async_smem();
-      mbar_arrive(&bar_k_ready);
-      for (int i = 0; i < n_q; ++i) {
-        const int q0 = w.seq_start + i * kTile;
-        const int q_rows = min(kTile, w.len - i * kTile);
-        int2 pq[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) pq[u] = (r + u * kRopeThreads < q_rows) ? pos[q0 + r + u * kRopeThreads] : make_int2(-1, -1);
-        if (!mbar_wait(&bar_q_full, i & 1, &s_abort)) break;
-        uint8_t* qt = smem + C::kOffQ;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int rr = r + u * kRopeThreads;
-          if (rr < q_rows) amax = fmaxf(amax, rope_row_to_f16<D>(qt, rr, pq[u], tab, args.scale_log2));
-          else zero_row<D>(qt, rr);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bar_q_ready);
-      }
+      mbar_arrive(&c.q_ready[s]);
+      return true;
+    };
+    bool ok = warp_wait(&c.kv_full, 0, abort_flag);
+    if (ok) {
+      uint8_t* kt = smem + C::kOffK;
+      if (r < kv_rows) amax = fmaxf(amax, rope_row_to_f16<D, kRopeUnroll>(kt, r, pos[kv0 + r], tab, 1.0f));
+      else zero_row<D>(kt, r);
+      fence_proxy_async_smem();
+      mbar_arrive(&c.k_ready);
+      ok = rope_q(0);
     }
-    if (!(amax <= kF16Max)) s_range = 1;
-  } else {
-    // Compute warpgroup: thread t owns K/V row t of the tile (TMEM lane t)
-    // for S^T, dP^T, dV, dk~, and query row t of the current Q tile for dQ.
-    const int t = tid;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float* s_row = reinterpret_cast<float*>(smem + C::kOffRow);  // [2][lse2 | D][128]
-    const bool kv_valid = t < kv_rows;
-    bool ok = true;
-    for (int i = 0; i < n_q; ++i) {
+    if (ok && n_q > 1) ok = rope_q(1);
+    for (int i = 0; ok && i < n_q; ++i) {
+      // dQ epilogue of Q tile i: TMEM B -> float atomics into the accumulator.
+      if (!warp_wait(&c.dq_full, i & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
       const int q0 = w.seq_start + i * kTile;
       const int q_rows = min(kTile, w.len - i * kTile);
-      float* lse2 = s_row + (i & 1) * 2 * kTile;
-      float* dsm = lse2 + kTile;
-      {
-        const bool vq = t < q_rows;
-        const size_t idx = static_cast<size_t>(w.head) * T + q0 + t;
-        lse2[t] = vq ? args.lse[idx] * kLog2e : 0.f;
-        dsm[t] = vq ? args.dsum[idx] : 0.f;
-      }
-      named_bar_sync(1, kComputeThreads);
-      if (!warp_wait(&bar_st_full, i & 1, &s_abort)) { ok = false; break; }
-      tc_fence_after();
-      uint8_t* Pt = smem + C::kOffP;
-      uint8_t* DSt = smem + C::kOffDS;
+      if (D == 128) {
+        // TMEM lane r = dimension r, column j = query j of the tile.
+        float* base = args.dq_acc + (static_cast<size_t>(q0) * args.g.heads + w.head) * D + r;
+        const size_t qstride = static_cast<size_t>(args.g.heads) * D;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], dp[32];
-        tmem_ld32(tl + C::kColS + c * 32, sv);
-        tmem_ld32(tl + C::kColDP + c * 32, dp);
-        tmem_wait_ld(sv);
-        tmem_wait_ld(dp);
-        uint32_t pw[16], dw[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qq = c * 32 + 2 * e + u;
-            const bool valid = kv_valid && qq < q_rows;
-            const float p = valid ? ex2_approx(__uint_as_float(sv[2 * e + u]) - lse2[qq]) : 0.f;
-            pv[u] = p;
-            dv[u] = valid ? p * (__uint_as_float(dp[2 * e + u]) - dsm[qq]) : 0.f;
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tl + C::kColB + 64 * hh, v0);
+          tmem_ld32(tl + C::kColB + 64 * hh + 32, v1);
+          tmem_wait_ld(v0);
+          tmem_wait_ld(v1);
+          if (hh == 1) {
+            tc_fence_before();
+            mbar_arrive(&c.dq_free);
           }
-          pw[e] = pack_bf16(pv[0], pv[1]);
-          dw[e] = pack_f16(dv[0], dv[1]);
+          const int nv = min(64, q_rows - 64 * hh);
+          float* ptr = base + static_cast<size_t>(64 * hh) * qstride;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            if (j < nv) atomicAdd(ptr, __uint_as_float(j < 32 ? v0[j] : v1[j - 32]));
+            ptr += qstride;
+          }
+        }
+      } else {
+        // TMEM lane r = query r of the tile, columns = dimensions.
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tl + C::kColB, v0);
+        tmem_ld32(tl + C::kColB + 32, v1);
+        tmem_wait_ld(v0);
+        tmem_wait_ld(v1);
+        tc_fence_before();
+        mbar_arrive(&c.dq_free);
+        if (r < q_rows) {
+          float4* dst = reinterpret_cast<float4*>(args.dq_acc + (static_cast<size_t>(q0 + r) * args.g.heads + w.head) * D);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            atomicAdd(dst + q, make_float4(__uint_as_float(v0[4 * q]), __uint_as_float(v0[4 * q + 1]),
+                                           __uint_as_float(v0[4 * q + 2]), __uint_as_float(v0[4 * q + 3])));
+            atomicAdd(dst + 8 + q, make_float4(__uint_as_float(v1[4 * q]), __uint_as_float(v1[4 * q + 1]),
+                                               __uint_as_float(v1[4 * q + 2]), __uint_as_float(v1[4 * q + 3])));
+          }
+        }
+      }
+      if (i + 2 < n_q) ok = rope_q(i + 2);
+    }
+    if (!(amax <= kF16Max)) c.range = 1;
+  } else {
+    regs_inc<kRegsCompute>();
+    // Thread r owns K/V row r (TMEM lane r); warpgroup cw the query columns
+    // 64cw .. 64cw + 63 of S^T / dP^T.
+    const int cw = wg;
+    const int r = tid & (kTile - 1);
+    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const bool kv_valid = r < kv_rows;
+    uint8_t* dst_ds = smem + C::kOffDS + cw * 16384;
+    bool ok = true;
+    for (int i = 0; i < n_q; ++i) {
+      const int s = i & 1;
+      if (!warp_wait(&c.q_ready[s], (i >> 1) & 1, abort_flag) || !warp_wait(&c.s_full, i & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float4* lse4 = reinterpret_cast<const float4*>(rowbuf + s * 2 * kTile + 64 * cw);
+      const float4* dsum4 = reinterpret_cast<const float4*>(rowbuf + s * 2 * kTile + kTile + 64 * cw);
+      float p[64];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        // query columns 64cw + 32hh .. + 31 -> packed TMEM columns 64cw + 16hh ..
+        uint32_t sv[32];
+        tmem_ld32(tl + C::kColA + 64 * cw + 32 * hh, sv);
+        tmem_wait_ld(sv);
+        uint32_t pw[16];
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 l = lse4[8 * hh + j4];
+          float* pp = p + 32 * hh + 4 * j4;
+          pp[0] = ex2_approx(__uint_as_float(sv[4 * j4 + 0]) - l.x);
+          pp[1] = ex2_approx(__uint_as_float(sv[4 * j4 + 1]) - l.y);
+          pp[2] = ex2_approx(__uint_as_float(sv[4 * j4 + 2]) - l.z);
+          pp[3] = ex2_approx(__uint_as_float(sv[4 * j4 + 3]) - l.w);
+          pw[2 * j4] = pack_bf16(pp[0], pp[1]);
+          pw[2 * j4 + 1] = pack_bf16(pp[2], pp[3]);
+        }
+        tmem_st16(tl + C::kColA + 64 * cw + 16 * hh, pw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&c.p_ready);
+      if (!warp_wait(&c.dp_full, i & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        // query columns 64cw + 32hh .. + 31 -> 16-byte chunks 4hh .. 4hh + 3
+        uint32_t dp[32];
+        tmem_ld32(tl + C::kColB + 64 * cw + 32 * hh, dp);
+        tmem_wait_ld(dp);
+        uint32_t dw[16];
+        if (kv_valid) {
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 d = dsum4[8 * hh + j4];
+            const float* pp = p + 32 * hh + 4 * j4;
+            dw[2 * j4] = pack_f16(pp[0] * (__uint_as_float(dp[4 * j4 + 0]) - d.x),
+                                  pp[1] * (__uint_as_float(dp[4 * j4 + 1]) - d.y));
+            dw[2 * j4 + 1] = pack_f16(pp[2] * (__uint_as_float(dp[4 * j4 + 2]) - d.z),
+                                      pp[3] * (__uint_as_float(dp[4 * j4 + 3]) - d.w));
+          }
+        } else {
+          // K/V rows past the sample's end: dS^T = 0 keeps them out of dQ.
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dw[j] = 0u;
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int ch = c * 4 + q;
-          const uint32_t off = (ch >> 3) * 16384 + sw128_off(t, ch & 7);
-          *reinterpret_cast<uint4*>(Pt + off) = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-          *reinterpret_cast<uint4*>(DSt + off) = make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
-        }
+        for (int ch = 0; ch < 4; ++ch)
+          *reinterpret_cast<uint4*>(dst_ds + sw128_off(r, 4 * hh + ch)) =
+              make_uint4(dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar_ds_ready);
-      if (!warp_wait(&bar_dq_full, i & 1, &s_abort)) { ok = false; break; }
-      tc_fence_after();
-      // dQ row t (query q0 + t) += TMEM lane t, columns 0..D-1.
-      float4* dst = reinterpret_cast<float4*>(args.dq_acc + (static_cast<size_t>(q0 + t) * args.g.heads + w.head) * D);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tl + C::kColDQ + c * 32, v);
-        tmem_wait_ld(v);
-        if (t < q_rows) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            atomicAdd(dst + c * 8 + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&bar_dq_free);
+      mbar_arrive(&c.ds_ready);
     }
-    if (ok && n_q > 0) {
-      // The last dq_full commit covers every MMA, so dV and dk~ are final.
+    if (ok && warp_wait(&c.fin, 0, abort_flag)) {
+      // Every MMA has completed: dV and dk~ are final.  Warpgroup cw stores
+      // columns cw * D/2 .. of its row.
       tc_fence_after();
-      const size_t rowoff = (static_cast<size_t>(kv0 + t) * args.g.heads + w.head) * D;
-      const int2 pk = kv_valid ? reinterpret_cast<const int2*>(args.g.pos)[kv0 + t] : make_int2(-1, -1);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      const size_t rowoff = (static_cast<size_t>(kv0 + r) * args.g.heads + w.head) * D;
+      const int2 pk = kv_valid ? reinterpret_cast<const int2*>(args.g.pos)[kv0 + r] : make_int2(-1, -1);
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int col0 = cw * (D / 2) + 32 * cc;
         uint32_t v[32];
-        tmem_ld32(tl + C::kColDV + c * 32, v);
+        tmem_ld32(tl + C::kColDV + col0, v);
         tmem_wait_ld(v);
         if (kv_valid)
-          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dv) + rowoff, v, c * 32, 1.0f, pk,
-                             args.g.rope_cs, false);
+          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dv) + rowoff, v, col0, 1.0f, pk, args.g.rope_cs,
+                             false);
       }
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int col0 = cw * (D / 2) + 32 * cc;
         uint32_t v[32];
-        tmem_ld32(tl + C::kColDK + c * 32, v);
+        tmem_ld32(tl + C::kColDK + col0, v);
         tmem_wait_ld(v);
         // TMEM holds dS^T (q~ * s * log2 e); dk~ = s dS^T q~ = ln 2 * TMEM.
         if (kv_valid)
-          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dk) + rowoff, v, c * 32, kLn2, pk,
-                             args.g.rope_cs, true);
+          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dk) + rowoff, v, col0, kLn2, pk, args.g.rope_cs,
+                             true);
       }
     }
   }
@@ -437,8 +577,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (tid == 0 && (s_abort || s_range))
-    atomicOr(args.g.status, (s_abort ? kStatusTimeout : 0) | (s_range ? kStatusRange : 0));
+  if (tid == 0 && (c.abort || c.range))
+    atomicOr(args.g.status, (c.abort ? kStatusTimeout : 0) | (c.range ? kStatusRange : 0));
 }
 
 template <int D>

@@ -63,7 +63,9 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
 // table entry i of rope_cs (float [grid][D/4][2] = cos, sin); text rows
 // (p.x < 0) are only scaled.  Returns the largest |value| written, so the
 // caller can flag values beyond the fp16 range.
-template <int D>
+// kUnroll bounds how many 16-byte chunks the compiler may keep in flight
+// (and so the registers the row needs).
+template <int D, int kUnroll = D / 8>
 __device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, const float* rope_cs,
                                                  float mult) {
   constexpr int nf = D / 4;
@@ -71,7 +73,7 @@ __device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, c
   if (p.x >= 0) {
     const float4* tab_row = reinterpret_cast<const float4*>(rope_cs) + static_cast<size_t>(p.x) * (nf / 2);
     const float4* tab_col = reinterpret_cast<const float4*>(rope_cs) + static_cast<size_t>(p.y) * (nf / 2);
-#pragma unroll
+#pragma unroll kUnroll
     for (int c16 = 0; c16 < D / 8; ++c16) {
       const int dim0 = c16 * 8;
       const int k0 = (dim0 % (D / 2)) / 2;  // multiple of 4
@@ -93,7 +95,7 @@ __device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, c
       *ptr = v;
     }
   } else {
-#pragma unroll
+#pragma unroll kUnroll
     for (int c16 = 0; c16 < D / 8; ++c16) {
       uint4* ptr = reinterpret_cast<uint4*>(tile + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7));
       uint4 v = *ptr;

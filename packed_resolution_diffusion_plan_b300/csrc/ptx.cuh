@@ -23,6 +23,9 @@ constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
 // Device status word bits (the host maps them to MF_ERR_TIMEOUT / MF_ERR_RANGE).
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusRange = 2;
+// A kernel found its shared-memory window misaligned for the swizzled tiles
+// and did no work.
+constexpr int kStatusLayout = 4;
 // Largest finite fp16 magnitude: the logit MMA's operands must stay below it.
 constexpr float kF16Max = 65504.0f;
 
@@ -201,6 +204,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
+// The same descriptor with the layout fields fixed at compile time, so only
+// the 32-bit address is live in registers.
+template <uint32_t kLbo, uint32_t kSbo>
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  constexpr uint64_t hi = (static_cast<uint64_t>((kLbo >> 4) & 0x3FFFu) << 16) |
+                          (static_cast<uint64_t>((kSbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+                          (static_cast<uint64_t>(2) << 61);
+  return hi | static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+}
+
 // Instruction descriptor, kind::f16 with fp32 accumulator; A and B are both
 // bf16 or both fp16 (never mixed).  a_mn / b_mn: operand stored MN-major
 // (transposed) instead of K-major.
@@ -228,6 +241,30 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Register rebalancing between warpgroups: every warp of a warpgroup runs the
+// same setmaxnreg; the shares of all warpgroups must add up to no more than
+// the registers the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]: A is M x 16 16-bit elements held as 8 TMEM
+// columns of packed pairs (lane = row, column c = elements 2c, 2c+1).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the mbarrier when every MMA issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
