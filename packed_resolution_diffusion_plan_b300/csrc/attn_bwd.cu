@@ -23,18 +23,19 @@
 //                           TMEM lane = dimension) so that a warp's float
 //                           atomics into the accumulator cover one 128-byte
 //                           line per query row
-//                issued in the order dV_i, dK_i, S^T_{i+1}, dQ_i, dP^T_{i+1},
-//                so the exponentials of tile i+1 overlap dQ_i and dP^T_{i+1}.
+//                issued in the order dV_i, dK_i, dQ_i, S^T_{i+1}, dP^T_{i+1}:
+//                the compute warps move dQ_i out of B while S^T_{i+1} runs.
 //                16 warps:
 //                  WG0, WG1  thread r owns K/V row r (TMEM lane r), WG c the
 //                            query columns 64c..64c+63: P^T = exp2(S^T - LSE2)
 //                            written back over its S^T columns as packed bf16,
 //                            dS^T = P^T * (dP^T - D) as fp16 into shared
-//                            memory; at the end dV and R^T dk~ to HBM
+//                            memory; the dQ epilogue (TMEM -> float atomics,
+//                            half the tile each); at the end dV and R^T dk~
 //                  WG2       RoPE of the K tile (once) and of every Q tile
 //                            (fp16, Q pre-scaled by s * log2 e so S^T is in
 //                            exp2 units), per-tile LSE2 / D rows into shared
-//                            memory; the dQ epilogue (TMEM -> float atomics)
+//                            memory
 //                  WG3       warp 12 TMA producer, warp 13 TMEM owner and MMA
 //                            issuer
 //   bwd_dq       dq = R^T (s * accumulator) as bf16.
@@ -51,7 +52,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 // Per-thread register shares after setmaxnreg; they add up to the launch's
 // 4 x 128 per thread.
-constexpr uint32_t kRegsCompute = 176, kRegsRope = 88, kRegsCtrl = 72;
+constexpr uint32_t kRegsCompute = 184, kRegsRope = 72, kRegsCtrl = 72;
 constexpr int kRopeUnroll = 4;
 static_assert(2 * kRegsCompute + kRegsRope + kRegsCtrl <= 4 * 128,
               "warpgroup register shares exceed the launch's registers");
@@ -226,7 +227,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     mbar_init(&c.ds_ready, 2 * kTile);
     mbar_init(&c.dv_done, 1);
     mbar_init(&c.dq_full, 1);
-    mbar_init(&c.dq_free, kTile);
+    mbar_init(&c.dq_free, 2 * kTile);
     c.abort = 0;
     c.range = 0;
     c.item = decode_item(args.g, blockIdx.x);
@@ -347,13 +348,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           mma_ss(tmem + C::kColDK, kmaj(sDS + off), mnmaj(sQ + s * C::kTileBytes + kk * 2048), id_dk, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&c.q_free[s]);
-        // S^T_{i+1} into A once dV_i has read P^T_i out of it.
-        if (more) {
-          if (!mbar_wait(&c.q_ready[s1], ph1, abort_flag) || !mbar_wait(&c.dv_done, ph, abort_flag)) break;
-          tc_fence_after();
-          issue_s(s1);
-          mma_commit(&c.s_full);
-        }
         // dQ_i into B (the compute warps have read dP^T_i before ds_ready).
 #pragma unroll 1
         for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -365,13 +359,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                    id_dq, kk > 0 ? 1u : 0u);
         }
         mma_commit(&c.dq_full);
-        // dP^T_{i+1} into B once the epilogue has read dQ_i out of it.
-        if (more) {
-          if (!mbar_wait(&c.do_full[s1], ph1, abort_flag) || !mbar_wait(&c.dq_free, ph, abort_flag)) break;
-          tc_fence_after();
-          issue_dp(s1);
-          mma_commit(&c.dp_full);
-        }
+        if (!more) break;
+        // S^T_{i+1} into A (dV_i has read P^T_i out of it); it runs while the
+        // compute warps move dQ_i out of B.
+        if (!mbar_wait(&c.q_ready[s1], ph1, abort_flag) || !mbar_wait(&c.dv_done, ph, abort_flag)) break;
+        tc_fence_after();
+        issue_s(s1);
+        mma_commit(&c.s_full);
+        // dP^T_{i+1} into B once dQ_i has been read out of it.
+        if (!mbar_wait(&c.do_full[s1], ph1, abort_flag) || !mbar_wait(&c.dq_free, ph, abort_flag)) break;
+        tc_fence_after();
+        issue_dp(s1);
+        mma_commit(&c.dp_full);
       }
       mma_commit(&c.fin);
       wait_drain(&c.fin, 0);
@@ -381,7 +380,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const int r = tid - kRopeWG * 128;
     const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
     const float* tab = args.g.rope_cs;
-    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     float amax = 0.f;
     // fp16 q~ * s * log2 e of row r of Q tile i, and that row's LSE2 / D.
     auto rope_q = [&](int i) -> bool {
@@ -411,58 +409,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       mbar_arrive(&c.k_ready);
       ok = rope_q(0);
     }
-    if (ok && n_q > 1) ok = rope_q(1);
-    for (int i = 0; ok && i < n_q; ++i) {
-      // dQ epilogue of Q tile i: TMEM B -> float atomics into the accumulator.
-      if (!warp_wait(&c.dq_full, i & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const int q0 = w.seq_start + i * kTile;
-      const int q_rows = min(kTile, w.len - i * kTile);
-      if (D == 128) {
-        // TMEM lane r = dimension r, column j = query j of the tile.
-        float* base = args.dq_acc + (static_cast<size_t>(q0) * args.g.heads + w.head) * D + r;
-        const size_t qstride = static_cast<size_t>(args.g.heads) * D;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t v0[32], v1[32];
-          tmem_ld32(tl + C::kColB + 64 * hh, v0);
-          tmem_ld32(tl + C::kColB + 64 * hh + 32, v1);
-          tmem_wait_ld(v0);
-          tmem_wait_ld(v1);
-          if (hh == 1) {
-            tc_fence_before();
-            mbar_arrive(&c.dq_free);
-          }
-          const int nv = min(64, q_rows - 64 * hh);
-          float* ptr = base + static_cast<size_t>(64 * hh) * qstride;
-#pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            if (j < nv) atomicAdd(ptr, __uint_as_float(j < 32 ? v0[j] : v1[j - 32]));
-            ptr += qstride;
-          }
-        }
-      } else {
-        // TMEM lane r = query r of the tile, columns = dimensions.
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tl + C::kColB, v0);
-        tmem_ld32(tl + C::kColB + 32, v1);
-        tmem_wait_ld(v0);
-        tmem_wait_ld(v1);
-        tc_fence_before();
-        mbar_arrive(&c.dq_free);
-        if (r < q_rows) {
-          float4* dst = reinterpret_cast<float4*>(args.dq_acc + (static_cast<size_t>(q0 + r) * args.g.heads + w.head) * D);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            atomicAdd(dst + q, make_float4(__uint_as_float(v0[4 * q]), __uint_as_float(v0[4 * q + 1]),
-                                           __uint_as_float(v0[4 * q + 2]), __uint_as_float(v0[4 * q + 3])));
-            atomicAdd(dst + 8 + q, make_float4(__uint_as_float(v1[4 * q]), __uint_as_float(v1[4 * q + 1]),
-                                               __uint_as_float(v1[4 * q + 2]), __uint_as_float(v1[4 * q + 3])));
-          }
-        }
-      }
-      if (i + 2 < n_q) ok = rope_q(i + 2);
-    }
+    for (int i = 1; ok && i < n_q; ++i) ok = rope_q(i);
     if (!(amax <= kF16Max)) c.range = 1;
   } else {
     regs_inc<kRegsCompute>();
@@ -473,9 +420,55 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const bool kv_valid = r < kv_rows;
     uint8_t* dst_ds = smem + C::kOffDS + cw * 16384;
+    // dQ of Q tile i (TMEM B) into the float accumulator; warpgroup cw takes
+    // half of it and releases B to the next dP^T as soon as its loads land.
+    auto dq_epilogue = [&](int i) -> bool {
+      if (!warp_wait(&c.dq_full, i & 1, abort_flag)) return false;
+      tc_fence_after();
+      const int q0 = w.seq_start + i * kTile;
+      const int q_rows = min(kTile, w.len - i * kTile);
+      if (D == 128) {
+        // TMEM lane r = dimension r, column j = query j of the tile.
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tl + C::kColB + 64 * cw, v0);
+        tmem_ld32(tl + C::kColB + 64 * cw + 32, v1);
+        tmem_wait_ld(v0);
+        tmem_wait_ld(v1);
+        tc_fence_before();
+        mbar_arrive(&c.dq_free);
+        const size_t qstride = static_cast<size_t>(args.g.heads) * D;
+        float* ptr = args.dq_acc + (static_cast<size_t>(q0 + 64 * cw) * args.g.heads + w.head) * D + r;
+        const int nv = min(64, q_rows - 64 * cw);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          if (j < nv) atomicAdd(ptr, __uint_as_float(j < 32 ? v0[j] : v1[j - 32]));
+          ptr += qstride;
+        }
+      } else {
+        // TMEM lane r = query r of the tile, columns = dimensions 32cw ..
+        uint32_t v[32];
+        tmem_ld32(tl + C::kColB + 32 * cw, v);
+        tmem_wait_ld(v);
+        tc_fence_before();
+        mbar_arrive(&c.dq_free);
+        if (r < q_rows) {
+          float4* dst =
+              reinterpret_cast<float4*>(args.dq_acc + (static_cast<size_t>(q0 + r) * args.g.heads + w.head) * D + 32 * cw);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            atomicAdd(dst + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+        }
+      }
+      return true;
+    };
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       const int s = i & 1;
+      if (i > 0 && !dq_epilogue(i - 1)) {
+        ok = false;
+        break;
+      }
       if (!warp_wait(&c.q_ready[s], (i >> 1) & 1, abort_flag) || !warp_wait(&c.s_full, i & 1, abort_flag)) {
         ok = false;
         break;
@@ -540,6 +533,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       tc_fence_before();
       mbar_arrive(&c.ds_ready);
     }
+    if (ok) ok = dq_epilogue(n_q - 1);
     if (ok && warp_wait(&c.fin, 0, abort_flag)) {
       // Every MMA has completed: dV and dk~ are final.  Warpgroup cw stores
       // columns cw * D/2 .. of its row.
