@@ -101,6 +101,9 @@ typedef struct {
   int32_t *cu_seqlens;  /* device int32 [n_samples + 1], exclusive scan of L_i */
   int32_t *pos;         /* device int32 [total_tokens][2]: (row, col); text = (-1, -1) */
   float *rope_cs;       /* device float32 [max_grid][head_dim/4][2]: cos, sin of p*f_i */
+  uint32_t *rope_cs16;  /* device [max_grid][head_dim/4] pairs of fp16 (cos low, sin high) of
+                           the same angles, each rounded once from double: the backward's
+                           copy, small enough to stay in the L1 cache next to its tiles */
   int32_t *order;       /* device int32 [n_samples][4]: (sample, first tile, first tile pair, 0),
                            longest sample first */
   int32_t *status;      /* device int32 status word written by kernels that time out */

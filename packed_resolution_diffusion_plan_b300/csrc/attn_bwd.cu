@@ -34,8 +34,9 @@
 //                            half the tile each); at the end dV and R^T dk~
 //                  WG2       RoPE of the K tile (once) and of every Q tile
 //                            (fp16, Q pre-scaled by s * log2 e so S^T is in
-//                            exp2 units), per-tile LSE2 / D rows into shared
-//                            memory
+//                            exp2 units) with the plan's fp16 cos/sin table,
+//                            which stays in L1; per-tile LSE2 / D rows into
+//                            shared memory
 //                  WG3       warp 12 TMA producer, warp 13 TMEM owner and MMA
 //                            issuer
 //   bwd_dq       dq = R^T (s * accumulator) as bf16.
@@ -297,7 +298,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       auto kmaj = [](uint32_t a) { return sdesc<16, 1024>(a); };
       auto mnmaj = [](uint32_t a) { return sdesc<16384, 1024>(a); };
       auto issue_s = [&](int s) {
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_ss(tmem + C::kColA, kmaj(sK + off), kmaj(sQ + s * C::kTileBytes + off),
@@ -305,7 +306,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
       };
       auto issue_dp = [&](int s) {
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_ss(tmem + C::kColB, kmaj(sV + off), kmaj(sDO + s * C::kTileBytes + off),
@@ -333,7 +334,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // warpgroup read its S^T from (query 64c.. at column 64c).
         if (!mbar_wait(&c.p_ready, ph, abort_flag)) break;
         tc_fence_after();
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(tmem + C::kColDV, tmem + C::kColA + 64 * (kk >> 2) + 8 * (kk & 3),
                  mnmaj(sDO + s * C::kTileBytes + kk * 2048), id_dv, (i > 0 || kk > 0) ? 1u : 0u);
@@ -342,14 +343,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // dk~ += dS^T_i q~_i
         if (!mbar_wait(&c.ds_ready, ph, abort_flag)) break;
         tc_fence_after();
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_ss(tmem + C::kColDK, kmaj(sDS + off), mnmaj(sQ + s * C::kTileBytes + kk * 2048), id_dk, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&c.q_free[s]);
         // dQ_i into B (the compute warps have read dP^T_i before ds_ready).
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           if (D == 128)
             mma_ss(tmem + C::kColB, mnmaj(sK + kk * 2048), mnmaj(sDS + kk * 2048),
@@ -379,7 +380,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     regs_dec<kRegsRope>();
     const int r = tid - kRopeWG * 128;
     const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
-    const float* tab = args.g.rope_cs;
+    const uint32_t* tab16 = args.g.rope_cs16;
     float amax = 0.f;
     // fp16 q~ * s * log2 e of row r of Q tile i, and that row's LSE2 / D.
     auto rope_q = [&](int i) -> bool {
@@ -392,7 +393,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       const float dd = valid ? args.dsum[idx] : 0.f;
       if (!warp_wait(&c.q_full[s], (i >> 1) & 1, abort_flag)) return false;
       uint8_t* qt = smem + C::kOffQ + s * C::kTileBytes;
-      if (valid) amax = fmaxf(amax, rope_row_to_f16<D, kRopeUnroll>(qt, r, p, tab, args.scale_log2));
+      if (valid) amax = fmaxf(amax, rope_row_to_f16_t16<D, kRopeUnroll>(qt, r, p, tab16, args.scale_log2));
       else zero_row<D>(qt, r);
       rowbuf[s * 2 * kTile + r] = l2;
       rowbuf[s * 2 * kTile + kTile + r] = dd;
@@ -403,7 +404,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     bool ok = warp_wait(&c.kv_full, 0, abort_flag);
     if (ok) {
       uint8_t* kt = smem + C::kOffK;
-      if (r < kv_rows) amax = fmaxf(amax, rope_row_to_f16<D, kRopeUnroll>(kt, r, pos[kv0 + r], tab, 1.0f));
+      if (r < kv_rows) amax = fmaxf(amax, rope_row_to_f16_t16<D, kRopeUnroll>(kt, r, pos[kv0 + r], tab16, 1.0f));
       else zero_row<D>(kt, r);
       fence_proxy_async_smem();
       mbar_arrive(&c.k_ready);

@@ -112,6 +112,56 @@ __device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, c
   return amax;
 }
 
+// The same rotation with the table's fp16 copy (rope_cs16: [grid][D/4] words
+// of fp16 cos | fp16 sin << 16): one 16-byte load covers the four pairs of a
+// 16-byte chunk, and the whole table of a 2048-pixel grid (16.5 KB) stays in
+// the L1 cache that the 226 KB of shared tiles leave.
+template <int D, int kUnroll = D / 8>
+__device__ __forceinline__ float rope_row_to_f16_t16(uint8_t* tile, int r, int2 p, const uint32_t* rope_cs16,
+                                                     float mult) {
+  constexpr int nf = D / 4;
+  float amax = 0.f;
+  if (p.x >= 0) {
+    const uint4* tab_row = reinterpret_cast<const uint4*>(rope_cs16) + static_cast<size_t>(p.x) * (nf / 4);
+    const uint4* tab_col = reinterpret_cast<const uint4*>(rope_cs16) + static_cast<size_t>(p.y) * (nf / 4);
+#pragma unroll kUnroll
+    for (int c16 = 0; c16 < D / 8; ++c16) {
+      const int dim0 = c16 * 8;
+      const int k0 = (dim0 % (D / 2)) / 2;  // multiple of 4
+      const uint4 t = __ldg((dim0 >= D / 2 ? tab_col : tab_row) + k0 / 4);
+      uint4* ptr = reinterpret_cast<uint4*>(tile + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7));
+      uint4 v = *ptr;
+      const uint32_t cs[4] = {t.x, t.y, t.z, t.w};
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&cs[e]));
+        const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
+        const float c = f.x * mult, s = f.y * mult;
+        const float y0 = fmaf(x0, c, -x1 * s), y1 = fmaf(x0, s, x1 * c);
+        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+        w[e] = pack_f16(y0, y1);
+      }
+      *ptr = v;
+    }
+  } else {
+#pragma unroll kUnroll
+    for (int c16 = 0; c16 < D / 8; ++c16) {
+      uint4* ptr = reinterpret_cast<uint4*>(tile + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7));
+      uint4 v = *ptr;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float y0 = bf16_lo(w[e]) * mult, y1 = bf16_hi(w[e]) * mult;
+        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+        w[e] = pack_f16(y0, y1);
+      }
+      *ptr = v;
+    }
+  }
+  return amax;
+}
+
 // Zero row r of a 128-row tile of D columns (rows past a sample's end).
 template <int D>
 __device__ __forceinline__ void zero_row(uint8_t* tile, int r) {

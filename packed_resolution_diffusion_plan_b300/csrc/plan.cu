@@ -5,6 +5,8 @@
 // MMDiT": variable-length latent token rows are packed back to back under a
 // fixed token budget and attention is confined by per-sample cumulative
 // offsets; section "Mage-VAE": an H x W px image becomes (H/16)(W/16) tokens.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace mf {
@@ -163,7 +165,8 @@ __global__ void pack_pos_kernel(PlanArgs a) {
 }
 
 // cos/sin(p * f_i), f_i = theta^(-2i/(head_dim/2)), i < head_dim/4.  The
-// angle and the sin/cos are evaluated in double and rounded to float once.
+// angle and the sin/cos are evaluated in double and rounded once, to float
+// for the float table and to fp16 for the 16-bit one.
 __global__ void rope_table_kernel(PlanArgs a) {
   const int nf = a.head_dim / 4;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
@@ -173,6 +176,8 @@ __global__ void rope_table_kernel(PlanArgs a) {
   double sv, cv;
   sincos(static_cast<double>(p) * f, &sv, &cv);
   reinterpret_cast<float2*>(a.rope_cs)[idx] = make_float2(static_cast<float>(cv), static_cast<float>(sv));
+  const __half hc = __double2half(cv), hs = __double2half(sv);
+  a.rope_cs16[idx] = static_cast<uint32_t>(__half_as_ushort(hc)) | (static_cast<uint32_t>(__half_as_ushort(hs)) << 16);
 }
 
 }  // namespace

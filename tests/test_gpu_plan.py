@@ -43,6 +43,10 @@ def _check_plan(samples, budget, head_dim=128, theta=10000.0):
         ang = np.arange(p.max_grid)[:, None] * f[None, :]
         assert np.abs(tab[..., 0] - np.cos(ang)).max() < 1e-7
         assert np.abs(tab[..., 1] - np.sin(ang)).max() < 1e-7
+        # the fp16 copy: the same values rounded once to fp16 (round to nearest even)
+        tab16 = p.rope_table16().cpu().numpy()
+        assert np.array_equal(tab16[..., 0], np.cos(ang).astype(np.float16))
+        assert np.array_equal(tab16[..., 1], np.sin(ang).astype(np.float16))
     return p
 
 
