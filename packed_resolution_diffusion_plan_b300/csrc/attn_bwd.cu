@@ -34,7 +34,7 @@
 //                            half the tile each); at the end dV and R^T dk~
 //                  WG2       RoPE of the K tile (once) and of every Q tile
 //                            (fp16, Q pre-scaled by s * log2 e so S^T is in
-//                            exp2 units) with the plan's fp16 cos/sin table,
+//                            exp2 units) from the plan's two-level table,
 //                            which stays in L1; per-tile LSE2 / D rows into
 //                            shared memory
 //                  WG3       warp 12 TMA producer, warp 13 TMEM owner and MMA
@@ -54,7 +54,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Per-thread register shares after setmaxnreg; they add up to the launch's
 // 4 x 128 per thread.
 constexpr uint32_t kRegsCompute = 184, kRegsRope = 72, kRegsCtrl = 72;
-constexpr int kRopeUnroll = 4;
+constexpr int kRopeUnroll = 2;
 static_assert(2 * kRegsCompute + kRegsRope + kRegsCtrl <= 4 * 128,
               "warpgroup register shares exceed the launch's registers");
 
@@ -380,7 +380,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     regs_dec<kRegsRope>();
     const int r = tid - kRopeWG * 128;
     const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
-    const uint32_t* tab16 = args.g.rope_cs16;
+    const float* tab_hl = args.g.rope_hl;
     float amax = 0.f;
     // fp16 q~ * s * log2 e of row r of Q tile i, and that row's LSE2 / D.
     auto rope_q = [&](int i) -> bool {
@@ -393,7 +393,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       const float dd = valid ? args.dsum[idx] : 0.f;
       if (!warp_wait(&c.q_full[s], (i >> 1) & 1, abort_flag)) return false;
       uint8_t* qt = smem + C::kOffQ + s * C::kTileBytes;
-      if (valid) amax = fmaxf(amax, rope_row_to_f16_t16<D, kRopeUnroll>(qt, r, p, tab16, args.scale_log2));
+      if (valid) amax = fmaxf(amax, rope_row_to_f16<D, true, kRopeUnroll>(qt, r, p, tab_hl, args.scale_log2));
       else zero_row<D>(qt, r);
       rowbuf[s * 2 * kTile + r] = l2;
       rowbuf[s * 2 * kTile + kTile + r] = dd;
@@ -404,7 +404,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     bool ok = warp_wait(&c.kv_full, 0, abort_flag);
     if (ok) {
       uint8_t* kt = smem + C::kOffK;
-      if (r < kv_rows) amax = fmaxf(amax, rope_row_to_f16_t16<D, kRopeUnroll>(kt, r, pos[kv0 + r], tab16, 1.0f));
+      if (r < kv_rows) amax = fmaxf(amax, rope_row_to_f16<D, false, kRopeUnroll>(kt, r, pos[kv0 + r], tab_hl, 1.0f));
       else zero_row<D>(kt, r);
       fence_proxy_async_smem();
       mbar_arrive(&c.k_ready);

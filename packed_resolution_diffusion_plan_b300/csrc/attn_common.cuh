@@ -59,35 +59,41 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
 
 // Row r of a 128-row bf16 tile of D columns (D/64 128-byte-swizzled halves)
 // becomes, in place, fp16 of  mult * R(p) x :  the first D/2 columns turn by
-// the latent row p.x, the rest by the column p.y, pair i of a half using
-// table entry i of rope_cs (float [grid][D/4][2] = cos, sin); text rows
-// (p.x < 0) are only scaled.  Returns the largest |value| written, so the
-// caller can flag values beyond the fp16 range.
-// kUnroll bounds how many 16-byte chunks the compiler may keep in flight
-// (and so the registers the row needs).
-template <int D, int kUnroll = D / 8>
-__device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, const float* rope_cs,
+// the latent row p.x, the rest by the column p.y, pair k of a half by angle
+// pos * f_k; text rows (p.x < 0) are only scaled.  The rotation of position
+// pos = 32 h + l is the product of the two-level table's entries
+// e^{i 32h f_k} and e^{i l f_k} (rope_hl, float [2][D/4][32][2]): 16 KB that
+// stay in L1 next to 226 KB of shared tiles, and a warp of consecutive
+// tokens reads consecutive l.  Returns the largest |value| written, so the
+// caller can flag values beyond the fp16 range.  kUnroll bounds the chunks
+// whose loads are in flight together (and so the registers the row needs).
+template <int D, bool kScale, int kUnroll = 2>
+__device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, const float* rope_hl,
                                                  float mult) {
   constexpr int nf = D / 4;
+  const float2* hi = reinterpret_cast<const float2*>(rope_hl);  // [nf][32]
+  const float2* lo = hi + nf * 32;                              // [nf][32]
   float amax = 0.f;
   if (p.x >= 0) {
-    const float4* tab_row = reinterpret_cast<const float4*>(rope_cs) + static_cast<size_t>(p.x) * (nf / 2);
-    const float4* tab_col = reinterpret_cast<const float4*>(rope_cs) + static_cast<size_t>(p.y) * (nf / 2);
+    const int hr = p.x >> 5, lr = p.x & 31, hc = p.y >> 5, lc = p.y & 31;
 #pragma unroll kUnroll
     for (int c16 = 0; c16 < D / 8; ++c16) {
-      const int dim0 = c16 * 8;
-      const int k0 = (dim0 % (D / 2)) / 2;  // multiple of 4
-      const float4* tab = dim0 >= D / 2 ? tab_col : tab_row;
-      const float4 a = __ldg(tab + k0 / 2);
-      const float4 b = __ldg(tab + k0 / 2 + 1);
+      const bool col_half = c16 >= D / 16;
+      const int k0 = ((c16 * 8) % (D / 2)) / 2;  // first pair of the chunk
+      const int h = col_half ? hc : hr, l = col_half ? lc : lr;
       uint4* ptr = reinterpret_cast<uint4*>(tile + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7));
       uint4 v = *ptr;
-      const float cs[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
       uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
+        const float2 A = __ldg(hi + (k0 + e) * 32 + h);
+        const float2 B = __ldg(lo + (k0 + e) * 32 + l);
+        float c = fmaf(A.x, B.x, -A.y * B.y), s = fmaf(A.y, B.x, A.x * B.y);
+        if (kScale) {
+          c *= mult;
+          s *= mult;
+        }
         const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
-        const float c = cs[2 * e] * mult, s = cs[2 * e + 1] * mult;
         const float y0 = fmaf(x0, c, -x1 * s), y1 = fmaf(x0, s, x1 * c);
         amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
         w[e] = pack_f16(y0, y1);
@@ -95,64 +101,15 @@ __device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, c
       *ptr = v;
     }
   } else {
-#pragma unroll kUnroll
+#pragma unroll 4
     for (int c16 = 0; c16 < D / 8; ++c16) {
       uint4* ptr = reinterpret_cast<uint4*>(tile + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7));
       uint4 v = *ptr;
       uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float y0 = bf16_lo(w[e]) * mult, y1 = bf16_hi(w[e]) * mult;
-        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
-        w[e] = pack_f16(y0, y1);
-      }
-      *ptr = v;
-    }
-  }
-  return amax;
-}
-
-// The same rotation with the table's fp16 copy (rope_cs16: [grid][D/4] words
-// of fp16 cos | fp16 sin << 16): one 16-byte load covers the four pairs of a
-// 16-byte chunk, and the whole table of a 2048-pixel grid (16.5 KB) stays in
-// the L1 cache that the 226 KB of shared tiles leave.
-template <int D, int kUnroll = D / 8>
-__device__ __forceinline__ float rope_row_to_f16_t16(uint8_t* tile, int r, int2 p, const uint32_t* rope_cs16,
-                                                     float mult) {
-  constexpr int nf = D / 4;
-  float amax = 0.f;
-  if (p.x >= 0) {
-    const uint4* tab_row = reinterpret_cast<const uint4*>(rope_cs16) + static_cast<size_t>(p.x) * (nf / 4);
-    const uint4* tab_col = reinterpret_cast<const uint4*>(rope_cs16) + static_cast<size_t>(p.y) * (nf / 4);
-#pragma unroll kUnroll
-    for (int c16 = 0; c16 < D / 8; ++c16) {
-      const int dim0 = c16 * 8;
-      const int k0 = (dim0 % (D / 2)) / 2;  // multiple of 4
-      const uint4 t = __ldg((dim0 >= D / 2 ? tab_col : tab_row) + k0 / 4);
-      uint4* ptr = reinterpret_cast<uint4*>(tile + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7));
-      uint4 v = *ptr;
-      const uint32_t cs[4] = {t.x, t.y, t.z, t.w};
-      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&cs[e]));
-        const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
-        const float c = f.x * mult, s = f.y * mult;
-        const float y0 = fmaf(x0, c, -x1 * s), y1 = fmaf(x0, s, x1 * c);
-        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
-        w[e] = pack_f16(y0, y1);
-      }
-      *ptr = v;
-    }
-  } else {
-#pragma unroll kUnroll
-    for (int c16 = 0; c16 < D / 8; ++c16) {
-      uint4* ptr = reinterpret_cast<uint4*>(tile + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7));
-      uint4 v = *ptr;
-      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float y0 = bf16_lo(w[e]) * mult, y1 = bf16_hi(w[e]) * mult;
+        const float y0 = kScale ? bf16_lo(w[e]) * mult : bf16_lo(w[e]);
+        const float y1 = kScale ? bf16_hi(w[e]) * mult : bf16_hi(w[e]);
         amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
         w[e] = pack_f16(y0, y1);
       }

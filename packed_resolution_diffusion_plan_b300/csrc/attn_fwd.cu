@@ -55,6 +55,7 @@ constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kRopeUnroll = 2;
 // Per-thread register shares after setmaxnreg (chosen from ptxas spill
 // reports: the producer/MMA warpgroup needs ~80, RoPE ~72-80).
 constexpr uint32_t kRegsSoftmax = 176, kRegsRope = 80, kRegsCtrl = 80;
@@ -206,7 +207,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     // sample's end are zeroed.
     const int r = tid - kRopeWG * 128;
     const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
-    const float* tab = args.g.rope_cs;
+    const float* tab_hl = args.g.rope_hl;
     float amax = 0.f;
     int2 pq[2];
 #pragma unroll
@@ -215,7 +216,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
       for (int a = 0; a < 2; ++a) {
         uint8_t* qt = smem + C::kOffQ + a * C::kTileBytes;
-        if (a * kTile + r < rows_left) amax = fmaxf(amax, rope_row_to_f16<D>(qt, r, pq[a], tab, args.scale_log2));
+        if (a * kTile + r < rows_left) amax = fmaxf(amax, rope_row_to_f16<D, true>(qt, r, pq[a], tab_hl, args.scale_log2));
         else zero_row<D>(qt, r);
       }
       fence_proxy_async_smem();
@@ -228,7 +229,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const int2 pk_next = (kr + kTile < w.len) ? pos[w.seq_start + kr + kTile] : make_int2(-1, -1);
         if (!mbar_wait(&bar_k_full[s], (j / C::kKStages) & 1, &s_abort)) break;
         uint8_t* kt = smem + C::kOffK + s * C::kTileBytes;
-        if (kr < w.len) amax = fmaxf(amax, rope_row_to_f16<D>(kt, r, pk, tab, 1.0f));
+        if (kr < w.len) amax = fmaxf(amax, rope_row_to_f16<D, false, kRopeUnroll>(kt, r, pk, tab_hl, 1.0f));
         else zero_row<D>(kt, r);
         fence_proxy_async_smem();
         mbar_arrive(&bar_k_rot[s]);

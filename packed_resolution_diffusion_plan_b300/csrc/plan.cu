@@ -5,8 +5,6 @@
 // MMDiT": variable-length latent token rows are packed back to back under a
 // fixed token budget and attention is confined by per-sample cumulative
 // offsets; section "Mage-VAE": an H x W px image becomes (H/16)(W/16) tokens.
-#include <cuda_fp16.h>
-
 #include "common.cuh"
 
 namespace mf {
@@ -164,20 +162,31 @@ __global__ void pack_pos_kernel(PlanArgs a) {
   reinterpret_cast<int2*>(a.pos)[tok] = p;
 }
 
-// cos/sin(p * f_i), f_i = theta^(-2i/(head_dim/2)), i < head_dim/4.  The
-// angle and the sin/cos are evaluated in double and rounded once, to float
-// for the float table and to fp16 for the 16-bit one.
+// cos/sin(p * f_i), f_i = theta^(-2i/(head_dim/2)), i < head_dim/4, for
+// p < grid_bound ([p][i] order), followed by the two-level table ([part][i][j]
+// order): part 0 at angle (32 j) f_i, part 1 at angle j f_i, j < 32.  Angles
+// and sin/cos are evaluated in double and rounded to float once.
 __global__ void rope_table_kernel(PlanArgs a) {
   const int nf = a.head_dim / 4;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= a.grid_bound * nf) return;
-  const int p = idx / nf, i = idx % nf;
+  const int n_full = a.grid_bound * nf;
+  if (idx >= n_full + 64 * nf) return;
+  int i, p;
+  if (idx < n_full) {
+    p = idx / nf;
+    i = idx % nf;
+  } else {
+    const int h = idx - n_full;  // [part][i][j]
+    const int part = h / (32 * nf);
+    i = (h / 32) % nf;
+    p = part == 0 ? 32 * (h % 32) : h % 32;
+  }
   const double f = pow(static_cast<double>(a.theta), -2.0 * i / (a.head_dim / 2));
   double sv, cv;
   sincos(static_cast<double>(p) * f, &sv, &cv);
-  reinterpret_cast<float2*>(a.rope_cs)[idx] = make_float2(static_cast<float>(cv), static_cast<float>(sv));
-  const __half hc = __double2half(cv), hs = __double2half(sv);
-  a.rope_cs16[idx] = static_cast<uint32_t>(__half_as_ushort(hc)) | (static_cast<uint32_t>(__half_as_ushort(hs)) << 16);
+  const float2 v = make_float2(static_cast<float>(cv), static_cast<float>(sv));
+  if (idx < n_full) reinterpret_cast<float2*>(a.rope_cs)[idx] = v;
+  else reinterpret_cast<float2*>(a.rope_hl)[idx - n_full] = v;
 }
 
 }  // namespace
@@ -191,8 +200,8 @@ cudaError_t launch_pack_plan(const PlanArgs& a, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int nt = a.grid_bound * (a.head_dim / 4);
-  if (nt > 0) {
+  const int nt = (a.grid_bound + 64) * (a.head_dim / 4);
+  if (a.grid_bound > 0) {
     rope_table_kernel<<<(nt + 255) / 256, 256, 0, stream>>>(a);
     e = cudaGetLastError();
   }
