@@ -133,6 +133,31 @@ mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t he
   return MF_OK;
 }
 
+// float32 [rows][heads][head_dim] view of the dQ accumulator as a 3D tensor
+// (dimension, head, token): boxes of head_dim x 1 x 64, no swizzle.
+mf_status make_tmap_acc(CUtensorMap* map, const float* base, int32_t rows, int32_t heads, int32_t head_dim) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    g_last_cuda_error = "cuTensorMapEncodeTiled entry point not available";
+    return MF_ERR_CUDA;
+  }
+  cuuint64_t gdim[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[2] = {static_cast<cuuint64_t>(head_dim) * 4, static_cast<cuuint64_t>(heads) * head_dim * 4};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(head_dim), 1, 64};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), gdim, gstride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[128];
+    snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled (dQ accumulator) failed with CUresult %d", static_cast<int>(r));
+    g_last_cuda_error = buf;
+    return MF_ERR_CUDA;
+  }
+  return MF_OK;
+}
+
 mf_status check_attn_common(const mf_plan* plan, int32_t heads, int32_t head_dim) {
   if (plan == nullptr || heads < 1) return MF_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
@@ -305,7 +330,9 @@ mf_status mf_attn_bwd(const void* q, const void* k, const void* v, const void* o
   a.dv = dv;
   cudaEvent_t ev0, ev1;
   take_events(&ev0, &ev1);
-  cudaError_t e = mf::launch_attn_bwd(a, tq, tk, tv, tdo, head_dim, static_cast<cudaStream_t>(stream), ev0, ev1);
+  CUtensorMap tdq;
+  if ((st = make_tmap_acc(&tdq, a.dq_acc, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  cudaError_t e = mf::launch_attn_bwd(a, tq, tk, tv, tdo, tdq, head_dim, static_cast<cudaStream_t>(stream), ev0, ev1);
   if (e != cudaSuccess) return cuda_fail(e, "mf_attn_bwd");
   return MF_OK;
 }

@@ -20,9 +20,8 @@
 //                  dk~   += dS^T_i q~_i      fp16, smem x smem
 //                  dQ_i   = dS_i k~          fp16, smem x smem -> B; with
 //                           head_dim 128 it is formed transposed (k~^T dS^T,
-//                           TMEM lane = dimension) so that a warp's float
-//                           atomics into the accumulator cover one 128-byte
-//                           line per query row
+//                           TMEM lane = dimension), so that a warp's stores
+//                           into the staging tile cover one 128-byte row
 //                issued in the order dV_i, dK_i, dQ_i, S^T_{i+1}, dP^T_{i+1}:
 //                the compute warps move dQ_i out of B while S^T_{i+1} runs.
 //                16 warps:
@@ -30,15 +29,20 @@
 //                            query columns 64c..64c+63: P^T = exp2(S^T - LSE2)
 //                            written back over its S^T columns as packed bf16,
 //                            dS^T = P^T * (dP^T - D) as fp16 into shared
-//                            memory; the dQ epilogue (TMEM -> float atomics,
+//                            memory; the dQ epilogue (TMEM -> staging tile,
 //                            half the tile each); at the end dV and R^T dk~
 //                  WG2       RoPE of the K tile (once) and of every Q tile
 //                            (fp16, Q pre-scaled by s * log2 e so S^T is in
 //                            exp2 units) from the plan's two-level table,
 //                            which stays in L1; per-tile LSE2 / D rows into
 //                            shared memory
-//                  WG3       warp 12 TMA producer, warp 13 TMEM owner and MMA
-//                            issuer
+//                  WG3       warp 12 TMA producer (Q ring of two, one dO
+//                            slot), warp 13 TMEM owner and MMA issuer, warp
+//                            14 the dQ reducer: with head_dim 128 each half of
+//                            dQ_i is staged in shared memory by its compute
+//                            warpgroup and added into the float accumulator
+//                            by one TMA reduce, so the compute warps never
+//                            wait on the reduction traffic
 //   bwd_dq       dq = R^T (s * accumulator) as bf16.
 #include "attn_common.cuh"
 
@@ -49,6 +53,7 @@ constexpr int kThreads = 16 * 32;
 constexpr int kRopeWG = 2;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
+constexpr int kReduceWarp = 14;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 // Per-thread register shares after setmaxnreg; they add up to the launch's
@@ -63,8 +68,9 @@ static_assert(2 * kRegsCompute + kRegsRope + kRegsCtrl <= 4 * 128,
 // base is the start of the CTA's window and the tiles stay 1024-aligned).
 struct BwdCtl {
   uint64_t kv_full, k_ready, fin;
-  uint64_t q_full[2], q_ready[2], q_free[2], do_full[2], do_free[2];
+  uint64_t q_full[2], q_ready[2], q_free[2], do_full, do_free;
   uint64_t s_full, p_ready, dp_full, ds_ready, dv_done, dq_full, dq_free;
+  uint64_t stage_full[2], stage_free[2];
   uint32_t tmem;
   int abort;
   int range;
@@ -80,9 +86,10 @@ struct BwdCfg {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
   static constexpr int kOffQ = kOffV + kTileBytes;       // 2 slots
-  static constexpr int kOffDO = kOffQ + 2 * kTileBytes;  // 2 slots
-  static constexpr int kOffDS = kOffDO + 2 * kTileBytes;
-  static constexpr int kOffRow = kOffDS + kSqBytes;      // [2 slots][LSE2[128] | D[128]] float
+  static constexpr int kOffDO = kOffQ + 2 * kTileBytes;  // 1 slot
+  static constexpr int kOffDS = kOffDO + kTileBytes;
+  static constexpr int kOffStage = kOffDS + kSqBytes;    // float [64 queries][D]: half a dQ tile
+  static constexpr int kOffRow = kOffStage + 64 * D * 4; // [2 slots][LSE2[128] | D[128]] float
   static constexpr int kOffCtl = kOffRow + 2 * 2 * kTile * 4;
   static constexpr int kDynSmem = kOffCtl + 256;
   static constexpr uint32_t kColA = 0, kColB = 128, kColDV = 256, kColDK = 256 + D;
@@ -197,7 +204,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                const BwdArgs args) {
+                const __grid_constant__ CUtensorMap tdq, const BwdArgs args) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   // The swizzled tiles need a 1024-byte aligned base; every thread sees the
@@ -219,9 +226,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       mbar_init(&c.q_full[s], 1);
       mbar_init(&c.q_ready[s], kTile);
       mbar_init(&c.q_free[s], 1);
-      mbar_init(&c.do_full[s], 1);
-      mbar_init(&c.do_free[s], 1);
+      mbar_init(&c.stage_full[s], kTile);
+      mbar_init(&c.stage_free[s], 1);
     }
+    mbar_init(&c.do_full, 1);
+    mbar_init(&c.do_free, 1);
     mbar_init(&c.s_full, 1);
     mbar_init(&c.p_ready, 2 * kTile);
     mbar_init(&c.dp_full, 1);
@@ -272,16 +281,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         for (int h = 0; h < C::kHalves; ++h)
           tma_load_2d(smem + C::kOffQ + s * C::kTileBytes + h * 16384, &tq, &c.q_full[s], xcol + h * 64, y);
         nq_issued = i + 1;
-        if (i >= 2 && !mbar_wait(&c.do_free[s], ph_free, abort_flag)) break;
-        mbar_arrive_expect_tx(&c.do_full[s], C::kTileBytes);
+        // dO_i reuses the one slot once dV_{i-1} has read dO_{i-1}.
+        if (i >= 1 && !mbar_wait(&c.do_free, (i - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&c.do_full, C::kTileBytes);
         for (int h = 0; h < C::kHalves; ++h)
-          tma_load_2d(smem + C::kOffDO + s * C::kTileBytes + h * 16384, &tdo, &c.do_full[s], xcol + h * 64, y);
+          tma_load_2d(smem + C::kOffDO + h * 16384, &tdo, &c.do_full, xcol + h * 64, y);
         ndo_issued = i + 1;
       }
       // Let this CTA's own copies land before its shared memory is released.
       wait_drain(&c.kv_full, 0);
       for (int j = max(0, nq_issued - 2); j < nq_issued; ++j) wait_drain(&c.q_full[j & 1], (j >> 1) & 1);
-      for (int j = max(0, ndo_issued - 2); j < ndo_issued; ++j) wait_drain(&c.do_full[j & 1], (j >> 1) & 1);
+      if (ndo_issued) wait_drain(&c.do_full, (ndo_issued - 1) & 1);
     } else if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t id_st = idesc_f16(kTile, kTile, false, false);   // k~ q~^T
       constexpr uint32_t id_dp = idesc_bf16(kTile, kTile, false, false);  // V dO^T
@@ -305,12 +315,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                  id_st, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_dp = [&](int s) {
+      auto issue_dp = [&]() {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kColB, kmaj(sV + off), kmaj(sDO + s * C::kTileBytes + off),
-                 id_dp, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::kColB, kmaj(sV + off), kmaj(sDO + off), id_dp, kk > 0 ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(&c.k_ready, 0, abort_flag) && mbar_wait(&c.kv_full, 0, abort_flag) &&
@@ -319,11 +328,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tc_fence_after();
         issue_s(0);
         mma_commit(&c.s_full);
-        ok = mbar_wait(&c.do_full[0], 0, abort_flag);
+        ok = mbar_wait(&c.do_full, 0, abort_flag);
       }
       if (ok) {
         tc_fence_after();
-        issue_dp(0);
+        issue_dp();
         mma_commit(&c.dp_full);
       }
       for (int i = 0; ok && i < n_q; ++i) {
@@ -337,9 +346,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(tmem + C::kColDV, tmem + C::kColA + 64 * (kk >> 2) + 8 * (kk & 3),
-                 mnmaj(sDO + s * C::kTileBytes + kk * 2048), id_dv, (i > 0 || kk > 0) ? 1u : 0u);
+                 mnmaj(sDO + kk * 2048), id_dv, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&c.dv_done);
-        mma_commit(&c.do_free[s]);
+        mma_commit(&c.do_free);
         // dk~ += dS^T_i q~_i
         if (!mbar_wait(&c.ds_ready, ph, abort_flag)) break;
         tc_fence_after();
@@ -368,13 +377,32 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         issue_s(s1);
         mma_commit(&c.s_full);
         // dP^T_{i+1} into B once dQ_i has been read out of it.
-        if (!mbar_wait(&c.do_full[s1], ph1, abort_flag) || !mbar_wait(&c.dq_free, ph, abort_flag)) break;
+        if (!mbar_wait(&c.do_full, (i + 1) & 1, abort_flag) || !mbar_wait(&c.dq_free, ph, abort_flag)) break;
         tc_fence_after();
-        issue_dp(s1);
+        issue_dp();
         mma_commit(&c.dp_full);
       }
       mma_commit(&c.fin);
       wait_drain(&c.fin, 0);
+    } else if (D == 128 && warp == kReduceWarp && lane == 0) {
+      // Reducer: each staged half of dQ_i (64 queries x D floats) is added
+      // into the accumulator by one TMA reduce; once the TMA has read it the
+      // other compute warpgroup may stage its half.
+      tma_prefetch_desc(&tdq);
+      bool ok = true;
+      for (int i = 0; ok && i < n_q; ++i) {
+        for (int cw = 0; cw < 2; ++cw) {
+          if (!mbar_wait(&c.stage_full[cw], i & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tma_reduce_add_3d(&tdq, smem + C::kOffStage, 0, w.head, w.seq_start + i * kTile + 64 * cw);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&c.stage_free[1 - cw]);
+        }
+      }
+      bulk_wait_group0();
     }
   } else if (wg == kRopeWG) {
     regs_dec<kRegsRope>();
@@ -422,14 +450,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const bool kv_valid = r < kv_rows;
     uint8_t* dst_ds = smem + C::kOffDS + cw * 16384;
     // dQ of Q tile i (TMEM B) into the float accumulator; warpgroup cw takes
-    // half of it and releases B to the next dP^T as soon as its loads land.
-    auto dq_epilogue = [&](int i) -> bool {
+    // half of it (queries 64cw ..) and releases B to the next dP^T as soon as
+    // its loads land.  With head_dim 128 the half is staged in shared memory
+    // (float [64 queries][D], TMEM lane r = dimension r) for the reducer's
+    // TMA reduce-add: warpgroup 0 stages right away, warpgroup 1 after the
+    // exponentials of the next tile, once the TMA has read warpgroup 0's half.
+    float dqv[64];
+    auto dq_load = [&](int i) -> bool {
       if (!warp_wait(&c.dq_full, i & 1, abort_flag)) return false;
       tc_fence_after();
-      const int q0 = w.seq_start + i * kTile;
-      const int q_rows = min(kTile, w.len - i * kTile);
       if (D == 128) {
-        // TMEM lane r = dimension r, column j = query j of the tile.
         uint32_t v0[32], v1[32];
         tmem_ld32(tl + C::kColB + 64 * cw, v0);
         tmem_ld32(tl + C::kColB + 64 * cw + 32, v1);
@@ -437,16 +467,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tmem_wait_ld(v1);
         tc_fence_before();
         mbar_arrive(&c.dq_free);
-        const size_t qstride = static_cast<size_t>(args.g.heads) * D;
-        float* ptr = args.dq_acc + (static_cast<size_t>(q0 + 64 * cw) * args.g.heads + w.head) * D + r;
-        const int nv = min(64, q_rows - 64 * cw);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          if (j < nv) atomicAdd(ptr, __uint_as_float(j < 32 ? v0[j] : v1[j - 32]));
-          ptr += qstride;
+        for (int j = 0; j < 32; ++j) {
+          dqv[j] = __uint_as_float(v0[j]);
+          dqv[32 + j] = __uint_as_float(v1[j]);
         }
       } else {
         // TMEM lane r = query r of the tile, columns = dimensions 32cw ..
+        const int q0 = w.seq_start + i * kTile;
+        const int q_rows = min(kTile, w.len - i * kTile);
         uint32_t v[32];
         tmem_ld32(tl + C::kColB + 32 * cw, v);
         tmem_wait_ld(v);
@@ -463,10 +492,22 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       }
       return true;
     };
+    auto dq_stage = [&](int i) -> bool {
+      if (D != 128) return true;
+      if (cw == 0 ? (i >= 1 && !warp_wait(&c.stage_free[0], (i - 1) & 1, abort_flag))
+                  : !warp_wait(&c.stage_free[1], i & 1, abort_flag))
+        return false;
+      float* st = reinterpret_cast<float*>(smem + C::kOffStage) + r;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) st[j * D] = dqv[j];
+      fence_proxy_async_smem();
+      mbar_arrive(&c.stage_full[cw]);
+      return true;
+    };
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       const int s = i & 1;
-      if (i > 0 && !dq_epilogue(i - 1)) {
+      if (i > 0 && (!dq_load(i - 1) || (cw == 0 && !dq_stage(i - 1)))) {
         ok = false;
         break;
       }
@@ -501,6 +542,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&c.p_ready);
+      if (i > 0 && cw == 1 && !dq_stage(i - 1)) { ok = false; break; }
       if (!warp_wait(&c.dp_full, i & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
@@ -534,7 +576,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       tc_fence_before();
       mbar_arrive(&c.ds_ready);
     }
-    if (ok) ok = dq_epilogue(n_q - 1);
+    if (ok) ok = dq_load(n_q - 1) && dq_stage(n_q - 1);
     if (ok && warp_wait(&c.fin, 0, abort_flag)) {
       // Every MMA has completed: dV and dk~ are final.  Warpgroup cw stores
       // columns cw * D/2 .. of its row.
@@ -578,7 +620,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, cudaStream_t stream, cudaEvent_t ev0,
+                         cudaEvent_t ev1) {
   using C = BwdCfg<D>;
   const long long chunks = static_cast<long long>(a.g.total_tokens) * a.g.heads * (D / 8);
   const int threads = 256;
@@ -589,7 +632,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
   e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return e;
-  bwd_main_kernel<D><<<a.g.n_items, kThreads, C::kDynSmem, stream>>>(tq, tk, tv, tdo, a);
+  bwd_main_kernel<D><<<a.g.n_items, kThreads, C::kDynSmem, stream>>>(tq, tk, tv, tdo, tdq, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return e;
@@ -600,11 +643,11 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
 }  // namespace
 
 cudaError_t launch_attn_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, int head_dim, cudaStream_t stream,
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, int head_dim, cudaStream_t stream,
                             cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   if (a.g.n_items <= 0) return cudaSuccess;
-  if (head_dim == 128) return launch_bwd_d<128>(a, tq, tk, tv, tdo, stream, ev_start, ev_stop);
-  return launch_bwd_d<64>(a, tq, tk, tv, tdo, stream, ev_start, ev_stop);
+  if (head_dim == 128) return launch_bwd_d<128>(a, tq, tk, tv, tdo, tdq, stream, ev_start, ev_stop);
+  return launch_bwd_d<64>(a, tq, tk, tv, tdo, tdq, stream, ev_start, ev_stop);
 }
 
 }  // namespace mf

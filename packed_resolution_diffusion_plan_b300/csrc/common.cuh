@@ -85,8 +85,10 @@ struct BwdArgs {
   void* dv;
 };
 
+// tdq: float32 [T][heads][D] view of the dQ accumulator, boxes of 64 tokens
+// of one head (used with head_dim 128).
 cudaError_t launch_attn_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, int head_dim,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq, int head_dim,
                             cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
 }  // namespace mf
