@@ -423,8 +423,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       uint8_t* qt = smem + C::kOffQ + s * C::kTileBytes;
       if (valid) amax = fmaxf(amax, rope_row_to_f16<D, true, kRopeUnroll>(qt, r, p, tab_hl, args.scale_log2));
       else zero_row<D>(qt, r);
-      rowbuf[s * 2 * kTile + r] = l2;
-      rowbuf[s * 2 * kTile + kTile + r] = dd;
+      // stored negated: P = exp2(S + (-LSE2)), dS = P * (dP + (-D)) on fp32 pairs
+      rowbuf[s * 2 * kTile + r] = -l2;
+      rowbuf[s * 2 * kTile + kTile + r] = -dd;
       fence_proxy_async_smem();
       mbar_arrive(&c.q_ready[s]);
       return true;
@@ -516,8 +517,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         break;
       }
       tc_fence_after();
-      const float4* lse4 = reinterpret_cast<const float4*>(rowbuf + s * 2 * kTile + 64 * cw);
-      const float4* dsum4 = reinterpret_cast<const float4*>(rowbuf + s * 2 * kTile + kTile + 64 * cw);
+      const float4* lse4 = reinterpret_cast<const float4*>(rowbuf + s * 2 * kTile + 64 * cw);          // -LSE2
+      const float4* dsum4 = reinterpret_cast<const float4*>(rowbuf + s * 2 * kTile + kTile + 64 * cw);  // -D
       float p[64];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -528,12 +529,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         uint32_t pw[16];
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 l = lse4[8 * hh + j4];
+          const float4 nl = lse4[8 * hh + j4];  // -LSE2 of four queries
           float* pp = p + 32 * hh + 4 * j4;
-          pp[0] = ex2_approx(__uint_as_float(sv[4 * j4 + 0]) - l.x);
-          pp[1] = ex2_approx(__uint_as_float(sv[4 * j4 + 1]) - l.y);
-          pp[2] = ex2_approx(__uint_as_float(sv[4 * j4 + 2]) - l.z);
-          pp[3] = ex2_approx(__uint_as_float(sv[4 * j4 + 3]) - l.w);
+          float x0, x1, x2, x3;
+          f2_unpack(f2_add(f2_pack(__uint_as_float(sv[4 * j4 + 0]), __uint_as_float(sv[4 * j4 + 1])),
+                           f2_pack(nl.x, nl.y)), x0, x1);
+          f2_unpack(f2_add(f2_pack(__uint_as_float(sv[4 * j4 + 2]), __uint_as_float(sv[4 * j4 + 3])),
+                           f2_pack(nl.z, nl.w)), x2, x3);
+          pp[0] = ex2_approx(x0);
+          pp[1] = ex2_approx(x1);
+          pp[2] = ex2_approx(x2);
+          pp[3] = ex2_approx(x3);
           pw[2 * j4] = pack_bf16(pp[0], pp[1]);
           pw[2 * j4 + 1] = pack_bf16(pp[2], pp[3]);
         }
@@ -555,12 +561,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         if (kv_valid) {
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 d = dsum4[8 * hh + j4];
+            const float4 nd = dsum4[8 * hh + j4];  // -D of four queries
             const float* pp = p + 32 * hh + 4 * j4;
-            dw[2 * j4] = pack_f16(pp[0] * (__uint_as_float(dp[4 * j4 + 0]) - d.x),
-                                  pp[1] * (__uint_as_float(dp[4 * j4 + 1]) - d.y));
-            dw[2 * j4 + 1] = pack_f16(pp[2] * (__uint_as_float(dp[4 * j4 + 2]) - d.z),
-                                      pp[3] * (__uint_as_float(dp[4 * j4 + 3]) - d.w));
+            float y0, y1, y2, y3;
+            f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dp[4 * j4 + 0]), __uint_as_float(dp[4 * j4 + 1])),
+                                    f2_pack(nd.x, nd.y)),
+                             f2_pack(pp[0], pp[1])),
+                      y0, y1);
+            f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dp[4 * j4 + 2]), __uint_as_float(dp[4 * j4 + 3])),
+                                    f2_pack(nd.z, nd.w)),
+                             f2_pack(pp[2], pp[3])),
+                      y2, y3);
+            dw[2 * j4] = pack_f16(y0, y1);
+            dw[2 * j4 + 1] = pack_f16(y2, y3);
           }
         } else {
           // K/V rows past the sample's end: dS^T = 0 keeps them out of dQ.

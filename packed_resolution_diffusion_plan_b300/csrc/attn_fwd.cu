@@ -262,11 +262,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           for (int i = 0; i < 32; ++i)
             if (c * 32 + i >= last_valid) sr[c][i] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // row max: three-input max into four independent chains
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+        for (int i = 0; i < 16; ++i)
+          m4[i & 3] = fmax3(m4[i & 3], __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
+      const float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
       const float m_new = fmaxf(m_run, mx);
       const bool need = m_new > m_run + kRescaleThreshold;
       const bool rescale_o = j > 0 && __any_sync(0xffffffffu, need);
@@ -276,22 +279,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         l_run *= alpha;
         m_run = m_new;
       }
-      const float neg_m = -m_run;
-      float rs = 0.f;
+      const uint64_t neg_m2 = f2_pack(-m_run, -m_run);
+      uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
       // P as packed bf16 pairs over S's first 64 columns (all of S is in
-      // registers already), 16 columns at a time so the logits die early.
+      // registers already), 16 columns at a time so the logits die early;
+      // S - m and the row sum run on fp32 pairs.
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(__uint_as_float(sr[c][2 * i]) + neg_m);
-          const float p1 = ex2_approx(__uint_as_float(sr[c][2 * i + 1]) + neg_m);
-          rs += p0 + p1;
+          float x0, x1;
+          f2_unpack(f2_add(f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), neg_m2), x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          rs2[i & 1] = f2_add(rs2[i & 1], f2_pack(p0, p1));
           pw[i] = pack_bf16(p0, p1);
         }
         tmem_st16(tl + colS + c * 16, pw);
       }
+      float rsa, rsb, rsc, rsd;
+      f2_unpack(rs2[0], rsa, rsb);
+      f2_unpack(rs2[1], rsc, rsd);
+      const float rs = (rsa + rsb) + (rsc + rsd);
       if (rescale_o) {
         // O_a is stable once PV_a(j-1) has completed; PV_a(j) is not issued
         // before p_full below.
