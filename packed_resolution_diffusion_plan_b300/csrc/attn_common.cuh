@@ -119,6 +119,91 @@ __device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, c
   return amax;
 }
 
+// The same rotation of row r with its 16-byte chunks software-pipelined:
+// chunk c + 1's row data and table entries are loaded before chunk c is
+// rotated and stored (the in-place store would otherwise order every later
+// load behind it), which roughly halves the row's latency at the cost of
+// ~100 registers; rows at or past the sample's end (valid = false) become
+// zero.  Used where the rotation of a streamed tile bounds the step (the
+// forward's K tiles).
+template <int D, bool kScale>
+__device__ __forceinline__ float rope_row_to_f16_pipelined(uint8_t* tile, int r, int2 p, bool valid,
+                                                           const float* rope_hl, float mult) {
+  constexpr int nf = D / 4;
+  constexpr int kChunks = D / 8;
+  const float2* hi = reinterpret_cast<const float2*>(rope_hl);  // [nf][32]
+  const float2* lo = hi + nf * 32;                              // [nf][32]
+  const uint32_t row_base = smem_u32(tile);
+  auto addr = [&](int c16) { return row_base + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7); };
+  float amax = 0.f;
+  if (!valid) {
+#pragma unroll
+    for (int c16 = 0; c16 < kChunks; ++c16) sts128(addr(c16), make_uint4(0, 0, 0, 0));
+    return 0.f;
+  }
+  if (p.x < 0) {
+#pragma unroll
+    for (int c16 = 0; c16 < kChunks; ++c16) {
+      uint4 v = lds128(addr(c16));
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float y0 = kScale ? bf16_lo(w[e]) * mult : bf16_lo(w[e]);
+        const float y1 = kScale ? bf16_hi(w[e]) * mult : bf16_hi(w[e]);
+        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+        w[e] = pack_f16(y0, y1);
+      }
+      sts128(addr(c16), v);
+    }
+    return amax;
+  }
+  const int hr = p.x >> 5, lr = p.x & 31, hc = p.y >> 5, lc = p.y & 31;
+  auto load = [&](int c16, uint4& v, float2 (&a)[4], float2 (&b)[4]) {
+    const bool col_half = c16 >= kChunks / 2;
+    const int k0 = ((c16 * 8) % (D / 2)) / 2;
+    const int h = col_half ? hc : hr, l = col_half ? lc : lr;
+    v = lds128(addr(c16));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      a[e] = __ldg(hi + (k0 + e) * 32 + h);
+      b[e] = __ldg(lo + (k0 + e) * 32 + l);
+    }
+  };
+  uint4 v_cur;
+  float2 a_cur[4], b_cur[4];
+  load(0, v_cur, a_cur, b_cur);
+#pragma unroll
+  for (int c16 = 0; c16 < kChunks; ++c16) {
+    uint4 v_nxt;
+    float2 a_nxt[4], b_nxt[4];
+    if (c16 + 1 < kChunks) load(c16 + 1, v_nxt, a_nxt, b_nxt);
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v_cur);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float c = fmaf(a_cur[e].x, b_cur[e].x, -a_cur[e].y * b_cur[e].y);
+      float s = fmaf(a_cur[e].y, b_cur[e].x, a_cur[e].x * b_cur[e].y);
+      if (kScale) {
+        c *= mult;
+        s *= mult;
+      }
+      const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
+      const float y0 = fmaf(x0, c, -x1 * s), y1 = fmaf(x0, s, x1 * c);
+      amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+      w[e] = pack_f16(y0, y1);
+    }
+    sts128(addr(c16), v_cur);
+    if (c16 + 1 < kChunks) {
+      v_cur = v_nxt;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        a_cur[e] = a_nxt[e];
+        b_cur[e] = b_nxt[e];
+      }
+    }
+  }
+  return amax;
+}
+
 // Zero row r of a 128-row tile of D columns (rows past a sample's end).
 template <int D>
 __device__ __forceinline__ void zero_row(uint8_t* tile, int r) {

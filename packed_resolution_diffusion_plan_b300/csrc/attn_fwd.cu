@@ -22,7 +22,9 @@
 //   WG3        warp 12: TMA producer (Q pair once; K into a 3-slot ring freed
 //              right after both logit MMAs, V into a 2-slot ring); warp 13:
 //              TMEM owner and single-thread MMA issuer:
-//                S_a = Q_a K_j^T (smem x smem), O_a += P_a V_j (P from TMEM)
+//                S_a = Q_a K_j^T (smem x smem), O_a += P_a V_j (P from TMEM),
+//              in the ping-pong order QK_0(j), PV_1(j-1), QK_1(j), PV_0(j),
+//              so one tile's softmax overlaps the other tile's MMAs
 // TMEM: S0 | S1 | O0 | O1 (128 + 128 + D + D columns of 512).  Registers are
 // rebalanced with setmaxnreg (the four warpgroup shares sum to the launch's
 // 4 x 128 per thread).
@@ -58,7 +60,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kRopeUnroll = 2;
 // Per-thread register shares after setmaxnreg (chosen from ptxas spill
 // reports: the producer/MMA warpgroup needs ~80, RoPE ~72-80).
-constexpr uint32_t kRegsSoftmax = 176, kRegsRope = 80, kRegsCtrl = 80;
+constexpr uint32_t kRegsSoftmax = 168, kRegsRope = 104, kRegsCtrl = 72;
 static_assert(2 * kRegsSoftmax + kRegsRope + kRegsCtrl <= 4 * 128,
               "warpgroup register shares exceed the launch's registers");
 
@@ -164,38 +166,65 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       const uint32_t sQ = smem_u32(smem + C::kOffQ);
       const uint32_t sK = smem_u32(smem + C::kOffK);
       const uint32_t sV = smem_u32(smem + C::kOffV);
-      bool ok = mbar_wait(&bar_q_ready, 0, &s_abort);
+      auto issue_qk = [&](int a, int j) {
+        const uint32_t kb = sK + (j % C::kKStages) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + C::kColS + a * kTile, sdesc<16, 1024>(sQ + a * C::kTileBytes + off), sdesc<16, 1024>(kb + off),
+                 idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_s_full[a]);
+      };
+      auto issue_pv = [&](int a, int j) {
+        const uint32_t vb = sV + (j % C::kVStages) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + C::kColO + a * D, tmem + C::kColS + a * kTile + kk * 8, sdesc<16384, 1024>(vb + kk * 2048),
+                 idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_pv_done[a]);
+      };
+      // Ping-pong order QK_0(j), PV_1(j-1), QK_1(j), PV_0(j), QK_0(j+1), ...:
+      // each tile's softmax overlaps the other tile's MMAs, and the two
+      // softmaxes never run at the same time.  S_a holds P_a until PV_a has
+      // read it, so QK_a waits for the tile's previous PV_a.
+      bool ok = mbar_wait(&bar_q_ready, 0, &s_abort) && mbar_wait(&bar_k_rot[0], 0, &s_abort);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0, 0);
+      }
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int sk = j % C::kKStages, sv = j % C::kVStages;
-        if (!mbar_wait(&bar_k_rot[sk], (j / C::kKStages) & 1, &s_abort)) { ok = false; break; }
-        for (int a = 0; a < 2 && ok; ++a) {
-          // S_a holds P_a(j-1) until PV_a(j-1) has read it.
-          if (j > 0 && !mbar_wait(&bar_pv_done[a], (j - 1) & 1, &s_abort)) { ok = false; break; }
+        if (j > 0) {
+          if (!mbar_wait(&bar_p_full[1], (j - 1) & 1, &s_abort)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + C::kColS + a * kTile, smem_desc(sQ + a * C::kTileBytes + off, 16, 1024),
-                   smem_desc(sK + sk * C::kTileBytes + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bar_s_full[a]);
-        }
-        if (!ok) break;
-        mma_commit(&bar_k_free[sk]);
-        for (int a = 0; a < 2 && ok; ++a) {
-          if (!mbar_wait(&bar_p_full[a], j & 1, &s_abort)) { ok = false; break; }
-          if (a == 0 && !mbar_wait(&bar_v_full[sv], (j / C::kVStages) & 1, &s_abort)) { ok = false; break; }
+          issue_pv(1, j - 1);
+          mma_commit(&bar_v_free[(j - 1) % C::kVStages]);
+          if (!mbar_wait(&bar_pv_done[1], (j - 1) & 1, &s_abort)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            mma_ts(tmem + C::kColO + a * D, tmem + C::kColS + a * kTile + kk * 8,
-                   smem_desc(sV + sv * C::kTileBytes + kk * 2048, 16384, 1024), idesc_pv,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bar_pv_done[a]);
         }
-        if (!ok) break;
-        mma_commit(&bar_v_free[sv]);
+        issue_qk(1, j);
+        mma_commit(&bar_k_free[j % C::kKStages]);
+        if (!mbar_wait(&bar_p_full[0], j & 1, &s_abort) ||
+            !mbar_wait(&bar_v_full[j % C::kVStages], (j / C::kVStages) & 1, &s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(0, j);
+        if (j + 1 < n_kv) {
+          if (!mbar_wait(&bar_k_rot[(j + 1) % C::kKStages], ((j + 1) / C::kKStages) & 1, &s_abort) ||
+              !mbar_wait(&bar_pv_done[0], j & 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_qk(0, j + 1);
+        }
+      }
+      if (ok && mbar_wait(&bar_p_full[1], (n_kv - 1) & 1, &s_abort)) {
+        tc_fence_after();
+        issue_pv(1, n_kv - 1);
+        mma_commit(&bar_v_free[(n_kv - 1) % C::kVStages]);
       }
       mma_commit(&bar_final);
       wait_drain(&bar_final, 0);
@@ -229,8 +258,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const int2 pk_next = (kr + kTile < w.len) ? pos[w.seq_start + kr + kTile] : make_int2(-1, -1);
         if (!mbar_wait(&bar_k_full[s], (j / C::kKStages) & 1, &s_abort)) break;
         uint8_t* kt = smem + C::kOffK + s * C::kTileBytes;
-        if (kr < w.len) amax = fmaxf(amax, rope_row_to_f16<D, false, kRopeUnroll>(kt, r, pk, tab_hl, 1.0f));
-        else zero_row<D>(kt, r);
+        amax = fmaxf(amax, rope_row_to_f16_pipelined<D, false>(kt, r, pk, kr < w.len, tab_hl, 1.0f));
         fence_proxy_async_smem();
         mbar_arrive(&bar_k_rot[s]);
         pk = pk_next;
