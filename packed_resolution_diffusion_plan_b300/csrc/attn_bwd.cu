@@ -31,9 +31,9 @@
 //                            dS^T = P^T * (dP^T - D) as fp16 into shared
 //                            memory; the dQ epilogue (TMEM -> staging tile,
 //                            half the tile each); at the end dV and R^T dk~
-//                  WG2       RoPE of the K tile (once) and of every Q tile
-//                            (fp16, Q pre-scaled by s * log2 e so S^T is in
-//                            exp2 units) from the plan's two-level table,
+//                  WG2       RoPE of the K tile (once, pre-scaled by
+//                            s * log2 e so S^T is in exp2 units) and of every
+//                            Q tile (fp16) from the plan's two-level table,
 //                            which stays in L1; per-tile LSE2 / D rows into
 //                            shared memory
 //                  WG3       warp 12 TMA producer (Q ring of two, one dO
@@ -131,7 +131,9 @@ __global__ void bwd_pre_kernel(const BwdArgs a) {
 }
 
 // ---------------------------------------------------------------- bwd_dq
-// dq = R^T (s * acc): one thread per (token, head, 8-column chunk).
+// dq = R^T (ln 2 * acc): the accumulator holds dS k~ with k~ pre-scaled by
+// s * log2 e, so s dS k~ = ln 2 * acc.  One thread per (token, head,
+// 8-column chunk).
 template <int D>
 __global__ void bwd_dq_kernel(const BwdArgs a) {
   constexpr int kChunks = D / 8;
@@ -157,12 +159,12 @@ __global__ void bwd_dq_kernel(const BwdArgs a) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float c = cs[2 * e], s = cs[2 * e + 1];
-      const float u0 = x[2 * e] * a.scale, u1 = x[2 * e + 1] * a.scale;
+      const float u0 = x[2 * e] * kLn2, u1 = x[2 * e + 1] * kLn2;
       out[e] = pack_bf16(fmaf(u0, c, u1 * s), fmaf(-u0, s, u1 * c));
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) out[e] = pack_bf16(x[2 * e] * a.scale, x[2 * e + 1] * a.scale);
+    for (int e = 0; e < 4; ++e) out[e] = pack_bf16(x[2 * e] * kLn2, x[2 * e + 1] * kLn2);
   }
   reinterpret_cast<uint4*>(a.dq)[gid] = make_uint4(out[0], out[1], out[2], out[3]);
 }
@@ -410,7 +412,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
     const float* tab_hl = args.g.rope_hl;
     float amax = 0.f;
-    // fp16 q~ * s * log2 e of row r of Q tile i, and that row's LSE2 / D.
+    // fp16 q~ of row r of Q tile i, and that row's LSE2 / D.
     auto rope_q = [&](int i) -> bool {
       const int s = i & 1;
       const int q0 = w.seq_start + i * kTile;
@@ -421,7 +423,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       const float dd = valid ? args.dsum[idx] : 0.f;
       if (!warp_wait(&c.q_full[s], (i >> 1) & 1, abort_flag)) return false;
       uint8_t* qt = smem + C::kOffQ + s * C::kTileBytes;
-      if (valid) amax = fmaxf(amax, rope_row_to_f16<D, true, kRopeUnroll>(qt, r, p, tab_hl, args.scale_log2));
+      if (valid) amax = fmaxf(amax, rope_row_to_f16<D, false, kRopeUnroll>(qt, r, p, tab_hl, 1.0f));
       else zero_row<D>(qt, r);
       // stored negated: P = exp2(S + (-LSE2)), dS = P * (dP + (-D)) on fp32 pairs
       rowbuf[s * 2 * kTile + r] = -l2;
@@ -433,7 +435,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     bool ok = warp_wait(&c.kv_full, 0, abort_flag);
     if (ok) {
       uint8_t* kt = smem + C::kOffK;
-      if (r < kv_rows) amax = fmaxf(amax, rope_row_to_f16<D, false, kRopeUnroll>(kt, r, pos[kv0 + r], tab_hl, 1.0f));
+      if (r < kv_rows)
+        amax = fmaxf(amax, rope_row_to_f16<D, true, kRopeUnroll>(kt, r, pos[kv0 + r], tab_hl, args.scale_log2));
       else zero_row<D>(kt, r);
       fence_proxy_async_smem();
       mbar_arrive(&c.k_ready);
@@ -612,10 +615,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         uint32_t v[32];
         tmem_ld32(tl + C::kColDK + col0, v);
         tmem_wait_ld(v);
-        // TMEM holds dS^T (q~ * s * log2 e); dk~ = s dS^T q~ = ln 2 * TMEM.
+        // TMEM holds dS^T q~; dk~ = s dS^T q~.
         if (kv_valid)
-          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dk) + rowoff, v, col0, kLn2, pk, args.g.rope_cs,
-                             true);
+          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dk) + rowoff, v, col0, args.scale, pk,
+                             args.g.rope_cs, true);
       }
     }
   }
