@@ -411,6 +411,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const int r = tid - kRopeWG * 128;
     const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
     const float* tab_hl = args.g.rope_hl;
+    const float* tab_cs = args.g.rope_cs;
     float amax = 0.f;
     // fp16 q~ of row r of Q tile i, and that row's LSE2 / D.
     auto rope_q = [&](int i) -> bool {
@@ -423,7 +424,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       const float dd = valid ? args.dsum[idx] : 0.f;
       if (!warp_wait(&c.q_full[s], (i >> 1) & 1, abort_flag)) return false;
       uint8_t* qt = smem + C::kOffQ + s * C::kTileBytes;
-      if (valid) amax = fmaxf(amax, rope_row_to_f16<D, false, kRopeUnroll>(qt, r, p, tab_hl, 1.0f));
+      if (valid) amax = fmaxf(amax, rope_row_to_f16<D, false, kRopeUnroll>(qt, r, p, tab_cs, tab_hl, 1.0f));
       else zero_row<D>(qt, r);
       // stored negated: P = exp2(S + (-LSE2)), dS = P * (dP + (-D)) on fp32 pairs
       rowbuf[s * 2 * kTile + r] = -l2;
@@ -436,7 +437,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     if (ok) {
       uint8_t* kt = smem + C::kOffK;
       if (r < kv_rows)
-        amax = fmaxf(amax, rope_row_to_f16<D, true, kRopeUnroll>(kt, r, pos[kv0 + r], tab_hl, args.scale_log2));
+        amax = fmaxf(amax, rope_row_to_f16<D, true, kRopeUnroll>(kt, r, pos[kv0 + r], tab_cs, tab_hl, args.scale_log2));
       else zero_row<D>(kt, r);
       fence_proxy_async_smem();
       mbar_arrive(&c.k_ready);

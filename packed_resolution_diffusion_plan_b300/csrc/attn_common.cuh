@@ -60,34 +60,54 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
 // Row r of a 128-row bf16 tile of D columns (D/64 128-byte-swizzled halves)
 // becomes, in place, fp16 of  mult * R(p) x :  the first D/2 columns turn by
 // the latent row p.x, the rest by the column p.y, pair k of a half by angle
-// pos * f_k; text rows (p.x < 0) are only scaled.  The rotation of position
-// pos = 32 h + l is the product of the two-level table's entries
+// pos * f_k; text rows (p.x < 0) are only scaled.  The first half reads the
+// full table (rope_cs, float [grid][D/4][2]) at p.x, which a whole image row
+// shares, so a warp's loads are broadcasts; the second half's rotation of
+// position pos = 32 h + l is the product of the two-level table's entries
 // e^{i 32h f_k} and e^{i l f_k} (rope_hl, float [2][D/4][32][2]): 16 KB that
 // stay in L1 next to 226 KB of shared tiles, and a warp of consecutive
 // tokens reads consecutive l.  Returns the largest |value| written, so the
 // caller can flag values beyond the fp16 range.  kUnroll bounds the chunks
 // whose loads are in flight together (and so the registers the row needs).
 template <int D, bool kScale, int kUnroll = 2>
-__device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, const float* rope_hl,
-                                                 float mult) {
+__device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, const float* rope_cs,
+                                                 const float* rope_hl, float mult) {
   constexpr int nf = D / 4;
   const float2* hi = reinterpret_cast<const float2*>(rope_hl);  // [nf][32]
   const float2* lo = hi + nf * 32;                              // [nf][32]
   float amax = 0.f;
   if (p.x >= 0) {
-    const int hr = p.x >> 5, lr = p.x & 31, hc = p.y >> 5, lc = p.y & 31;
+    const float2* full = reinterpret_cast<const float2*>(rope_cs) + static_cast<size_t>(p.x) * nf;
+    const int hc = p.y >> 5, lc = p.y & 31;
+    // first half: one full-table entry per pair
 #pragma unroll kUnroll
-    for (int c16 = 0; c16 < D / 8; ++c16) {
-      const bool col_half = c16 >= D / 16;
-      const int k0 = ((c16 * 8) % (D / 2)) / 2;  // first pair of the chunk
-      const int h = col_half ? hc : hr, l = col_half ? lc : lr;
+    for (int c16 = 0; c16 < D / 16; ++c16) {
+      const int k0 = c16 * 4;
       uint4* ptr = reinterpret_cast<uint4*>(tile + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7));
       uint4 v = *ptr;
       uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 A = __ldg(hi + (k0 + e) * 32 + h);
-        const float2 B = __ldg(lo + (k0 + e) * 32 + l);
+        const float2 F = __ldg(full + k0 + e);
+        const float c = kScale ? F.x * mult : F.x, s = kScale ? F.y * mult : F.y;
+        const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
+        const float y0 = fmaf(x0, c, -x1 * s), y1 = fmaf(x0, s, x1 * c);
+        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+        w[e] = pack_f16(y0, y1);
+      }
+      *ptr = v;
+    }
+    // second half: the product of the two-level table's entries
+#pragma unroll kUnroll
+    for (int c16 = D / 16; c16 < D / 8; ++c16) {
+      const int k0 = (c16 - D / 16) * 4;
+      uint4* ptr = reinterpret_cast<uint4*>(tile + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7));
+      uint4 v = *ptr;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 A = __ldg(hi + (k0 + e) * 32 + hc);
+        const float2 B = __ldg(lo + (k0 + e) * 32 + lc);
         float c = fmaf(A.x, B.x, -A.y * B.y), s = fmaf(A.y, B.x, A.x * B.y);
         if (kScale) {
           c *= mult;
@@ -128,7 +148,7 @@ __device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, c
 // forward's K tiles).
 template <int D, bool kScale>
 __device__ __forceinline__ float rope_row_to_f16_pipelined(uint8_t* tile, int r, int2 p, bool valid,
-                                                           const float* rope_hl, float mult) {
+                                                           const float* rope_cs, const float* rope_hl, float mult) {
   constexpr int nf = D / 4;
   constexpr int kChunks = D / 8;
   const float2* hi = reinterpret_cast<const float2*>(rope_hl);  // [nf][32]
@@ -157,16 +177,22 @@ __device__ __forceinline__ float rope_row_to_f16_pipelined(uint8_t* tile, int r,
     }
     return amax;
   }
-  const int hr = p.x >> 5, lr = p.x & 31, hc = p.y >> 5, lc = p.y & 31;
+  const float2* full = reinterpret_cast<const float2*>(rope_cs) + static_cast<size_t>(p.x) * nf;
+  const int hc = p.y >> 5, lc = p.y & 31;
+  // first half: (cos, sin) from the full table at p.x; second half: the two
+  // two-level factors of p.y
   auto load = [&](int c16, uint4& v, float2 (&a)[4], float2 (&b)[4]) {
-    const bool col_half = c16 >= kChunks / 2;
     const int k0 = ((c16 * 8) % (D / 2)) / 2;
-    const int h = col_half ? hc : hr, l = col_half ? lc : lr;
     v = lds128(addr(c16));
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      a[e] = __ldg(hi + (k0 + e) * 32 + h);
-      b[e] = __ldg(lo + (k0 + e) * 32 + l);
+      if (c16 >= kChunks / 2) {
+        a[e] = __ldg(hi + (k0 + e) * 32 + hc);
+        b[e] = __ldg(lo + (k0 + e) * 32 + lc);
+      } else {
+        a[e] = __ldg(full + k0 + e);
+        b[e] = make_float2(1.f, 0.f);
+      }
     }
   };
   uint4 v_cur;
@@ -180,8 +206,11 @@ __device__ __forceinline__ float rope_row_to_f16_pipelined(uint8_t* tile, int r,
     uint32_t* w = reinterpret_cast<uint32_t*>(&v_cur);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      float c = fmaf(a_cur[e].x, b_cur[e].x, -a_cur[e].y * b_cur[e].y);
-      float s = fmaf(a_cur[e].y, b_cur[e].x, a_cur[e].x * b_cur[e].y);
+      float c = a_cur[e].x, s = a_cur[e].y;
+      if (c16 >= kChunks / 2) {
+        c = fmaf(a_cur[e].x, b_cur[e].x, -a_cur[e].y * b_cur[e].y);
+        s = fmaf(a_cur[e].y, b_cur[e].x, a_cur[e].x * b_cur[e].y);
+      }
       if (kScale) {
         c *= mult;
         s *= mult;

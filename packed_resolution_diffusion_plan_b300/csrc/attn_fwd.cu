@@ -237,6 +237,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const int r = tid - kRopeWG * 128;
     const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
     const float* tab_hl = args.g.rope_hl;
+    const float* tab_cs = args.g.rope_cs;
     float amax = 0.f;
     int2 pq[2];
 #pragma unroll
@@ -245,7 +246,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
       for (int a = 0; a < 2; ++a) {
         uint8_t* qt = smem + C::kOffQ + a * C::kTileBytes;
-        if (a * kTile + r < rows_left) amax = fmaxf(amax, rope_row_to_f16<D, true>(qt, r, pq[a], tab_hl, args.scale_log2));
+        if (a * kTile + r < rows_left) amax = fmaxf(amax, rope_row_to_f16<D, true>(qt, r, pq[a], tab_cs, tab_hl, args.scale_log2));
         else zero_row<D>(qt, r);
       }
       fence_proxy_async_smem();
@@ -258,7 +259,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const int2 pk_next = (kr + kTile < w.len) ? pos[w.seq_start + kr + kTile] : make_int2(-1, -1);
         if (!mbar_wait(&bar_k_full[s], (j / C::kKStages) & 1, &s_abort)) break;
         uint8_t* kt = smem + C::kOffK + s * C::kTileBytes;
-        amax = fmaxf(amax, rope_row_to_f16_pipelined<D, false>(kt, r, pk, kr < w.len, tab_hl, 1.0f));
+        amax = fmaxf(amax, rope_row_to_f16_pipelined<D, false>(kt, r, pk, kr < w.len, tab_cs, tab_hl, 1.0f));
         fence_proxy_async_smem();
         mbar_arrive(&bar_k_rot[s]);
         pk = pk_next;
