@@ -109,8 +109,10 @@ EncodeTiledFn encode_fn() {
 }
 
 // [rows, heads*head_dim] bf16 view of a [T, heads, head_dim] tensor; boxes of
-// 128 rows x 64 columns, 128-byte swizzle, zero fill past the last row.
-mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t heads, int32_t head_dim) {
+// box_rows (128 or 64) rows x 64 columns, 128-byte swizzle, zero fill past
+// the last row.
+mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t heads, int32_t head_dim,
+                    uint32_t box_rows = mf::kTile) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     g_last_cuda_error = "cuTensorMapEncodeTiled entry point not available";
@@ -119,7 +121,7 @@ mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t he
   const cuuint64_t cols = static_cast<cuuint64_t>(heads) * head_dim;
   cuuint64_t gdim[2] = {cols, static_cast<cuuint64_t>(rows)};
   cuuint64_t gstride[1] = {cols * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mf::kTile)};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estride[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
                    estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -311,13 +313,16 @@ mf_status mf_attn_bwd(const void* q, const void* k, const void* v, const void* o
   if ((st = mf_attn_bwd_workspace_size(plan->total_tokens, heads, head_dim, &need)) != MF_OK) return st;
   if (workspace_bytes < need) return MF_ERR_INVALID_ARG;
   CUtensorMap tq, tk, tv, tdo;
-  if ((st = make_tmap(&tq, q, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  // Q is loaded in 64-row halves (each CTA of a cluster rotates one half).
+  if ((st = make_tmap(&tq, q, plan->total_tokens, heads, head_dim, 64)) != MF_OK) return st;
   if ((st = make_tmap(&tk, k, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   if ((st = make_tmap(&tdo, dout, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   const size_t rows = static_cast<size_t>(plan->total_tokens) * heads;
   mf::BwdArgs a;
   a.g = make_geom(plan, heads);
+  // clusters of two CTAs over pairs of K/V tiles (the forward's 256-row units)
+  a.g.n_items = 2 * plan->n_pairs * heads;
   a.scale = resolve_scale(softmax_scale, head_dim);
   a.scale_log2 = a.scale * kLog2e;
   a.o = o;

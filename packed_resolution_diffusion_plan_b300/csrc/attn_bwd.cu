@@ -11,7 +11,12 @@
 //   bwd_pre      D = rowsum(dO * O) (float32 [heads, T]); zero the float32 dQ
 //                accumulator.
 //   bwd_main     one CTA per (sample, head, 128-row K/V tile), streaming the
-//                sample's 128-row Q/dO tiles through two-slot rings.  Per Q
+//                sample's 128-row Q/dO tiles (a two-slot Q ring, one dO
+//                slot).  CTAs run in clusters of two over K/V tiles 2p and
+//                2p + 1, which stream the same Q tiles: each loads and rotates
+//                64 rows of every Q tile (a half row per RoPE thread) and
+//                stores them into both CTAs' shared memory, halving the
+//                rotation work per CTA.  Per Q
 //                tile i, five tcgen05 MMAs (TMEM columns: A = 0..127,
 //                B = 128..255, dV = 256.., dK = 256 + D..):
 //                  S^T_i  = k~ q~_i^T        fp16, smem x smem -> A
@@ -59,7 +64,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Per-thread register shares after setmaxnreg; they add up to the launch's
 // 4 x 128 per thread.
 constexpr uint32_t kRegsCompute = 184, kRegsRope = 72, kRegsCtrl = 72;
-constexpr int kRopeUnroll = 2;
+constexpr int kRopeUnroll = 2;  // K tile rotation (once per CTA)
 static_assert(2 * kRegsCompute + kRegsRope + kRegsCtrl <= 4 * 128,
               "warpgroup register shares exceed the launch's registers");
 
@@ -203,7 +208,7 @@ __device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                 const __grid_constant__ CUtensorMap tdq, const BwdArgs args) {
@@ -220,14 +225,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   volatile int* abort_flag = &c.abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
+  // The two CTAs of a cluster own consecutive K/V tiles 2p and 2p + 1 of one
+  // (sample, head) and stream the same Q tiles: each loads and rotates half
+  // of every Q tile's rows and writes them into both CTAs' shared memory.
+  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   if (tid == 0) {
     mbar_init(&c.kv_full, 1);
     mbar_init(&c.k_ready, kTile);
     mbar_init(&c.fin, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&c.q_full[s], 1);
-      mbar_init(&c.q_ready[s], kTile);
-      mbar_init(&c.q_free[s], 1);
+      mbar_init(&c.q_ready[s], kTile);  // this CTA's RoPE threads, plus the peer's half as tx bytes
+      mbar_init(&c.q_free[s], 2);           // both CTAs' MMAs are done with the slot
       mbar_init(&c.stage_full[s], kTile);
       mbar_init(&c.stage_free[s], 1);
     }
@@ -242,7 +251,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     mbar_init(&c.dq_free, 2 * kTile);
     c.abort = 0;
     c.range = 0;
-    c.item = decode_item(args.g, blockIdx.x);
+    c.item = decode_item<2 * kTile>(args.g, blockIdx.x >> 1);  // tile = K/V tile pair
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -250,13 +259,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrival
   tc_fence_after();
 
   const uint32_t tmem = c.tmem;
-  const WorkItem w = c.item;             // w.tile = this CTA's K/V tile
-  const int kv0 = w.seq_start + w.tile * kTile;
-  const int kv_rows = min(kTile, w.len - w.tile * kTile);
+  const WorkItem w = c.item;
+  const int kv_tile = 2 * w.tile + static_cast<int>(rank);
+  // An odd tile count leaves the last pair's second CTA without rows: it
+  // still shares the Q rotation, and its K/V rows all count as invalid.
+  const int kv0 = w.seq_start + kv_tile * kTile;
+  const int kv_rows = max(0, min(kTile, w.len - kv_tile * kTile));
   const int n_q = (w.len + kTile - 1) / kTile;
   const int xcol = w.head * D;
   const int T = args.g.total_tokens;
@@ -279,9 +291,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const uint32_t ph_free = ((i >> 1) - 1) & 1;  // completion i/2 - 1 of the slot's free barrier
         const int y = w.seq_start + i * kTile;
         if (i >= 2 && !mbar_wait(&c.q_free[s], ph_free, abort_flag)) break;
-        mbar_arrive_expect_tx(&c.q_full[s], C::kTileBytes);
+        // this CTA's 64 rows of Q_i (rank r: rows 64r ..); the peer writes the other half, rotated
+        mbar_arrive_expect_tx(&c.q_full[s], C::kTileBytes / 2);
         for (int h = 0; h < C::kHalves; ++h)
-          tma_load_2d(smem + C::kOffQ + s * C::kTileBytes + h * 16384, &tq, &c.q_full[s], xcol + h * 64, y);
+          tma_load_2d(smem + C::kOffQ + s * C::kTileBytes + h * 16384 + rank * 8192, &tq, &c.q_full[s], xcol + h * 64,
+                      y + 64 * static_cast<int>(rank));
         nq_issued = i + 1;
         // dO_i reuses the one slot once dV_{i-1} has read dO_{i-1}.
         if (i >= 1 && !mbar_wait(&c.do_free, (i - 1) & 1, abort_flag)) break;
@@ -359,7 +373,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_ss(tmem + C::kColDK, kmaj(sDS + off), mnmaj(sQ + s * C::kTileBytes + kk * 2048), id_dk, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&c.q_free[s]);
+        mma_commit_multicast(&c.q_free[s], 0x3);  // frees the slot in both CTAs' accounting
         // dQ_i into B (the compute warps have read dP^T_i before ds_ready).
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -414,23 +428,41 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const float* tab_cs = args.g.rope_cs;
     float amax = 0.f;
     // fp16 q~ of row r of Q tile i, and that row's LSE2 / D.
+    // Threads 2j and 2j + 1 share row 64 * rank + j of each Q tile, each
+    // rotating the same share of both halves; the rotated rows are copied
+    // into the peer CTA's tile.
+    const int rr = 64 * static_cast<int>(rank) + (r >> 1), part = r & 1;
     auto rope_q = [&](int i) -> bool {
       const int s = i & 1;
       const int q0 = w.seq_start + i * kTile;
       const bool valid = r < w.len - i * kTile;
+      const bool valid_rr = rr < w.len - i * kTile;
       const size_t idx = static_cast<size_t>(w.head) * T + q0 + r;
-      const int2 p = valid ? pos[q0 + r] : make_int2(-1, -1);
+      const int2 p = valid_rr ? pos[q0 + rr] : make_int2(-1, -1);
       const float l2 = valid ? args.lse[idx] * kLog2e : INFINITY;  // invalid query: P = 0
       const float dd = valid ? args.dsum[idx] : 0.f;
       if (!warp_wait(&c.q_full[s], (i >> 1) & 1, abort_flag)) return false;
       uint8_t* qt = smem + C::kOffQ + s * C::kTileBytes;
-      if (valid) amax = fmaxf(amax, rope_row_to_f16<D, false, kRopeUnroll>(qt, r, p, tab_cs, tab_hl, 1.0f));
-      else zero_row<D>(qt, r);
+      amax = fmaxf(amax, rope_part_row_to_f16<D, false, 2>(qt, rr, part, p, valid_rr, tab_cs, tab_hl, 1.0f));
       // stored negated: P = exp2(S + (-LSE2)), dS = P * (dP + (-D)) on fp32 pairs
       rowbuf[s * 2 * kTile + r] = -l2;
       rowbuf[s * 2 * kTile + kTile + r] = -dd;
       fence_proxy_async_smem();
-      mbar_arrive(&c.q_ready[s]);
+      // Once the whole half is rotated, one thread copies it into the peer's
+      // slot (the peer freed it: q_free counts both CTAs' MMAs), completing
+      // on the peer's q_ready as transaction bytes; this CTA's q_ready
+      // expects the peer's half the same way.
+      named_bar_sync(3, kTile);
+      if (r == 0) {
+        const uint32_t bar_peer = mapa_shared(smem_u32(&c.q_ready[s]), peer);
+        for (int h = 0; h < C::kHalves; ++h) {
+          uint8_t* src = qt + h * 16384 + rank * 8192;
+          bulk_copy_to_cluster(mapa_shared(smem_u32(src), peer), src, 8192, bar_peer);
+        }
+        mbar_arrive_expect_tx(&c.q_ready[s], C::kTileBytes / 2);
+      } else {
+        mbar_arrive(&c.q_ready[s]);
+      }
       return true;
     };
     bool ok = warp_wait(&c.kv_full, 0, abort_flag);
@@ -625,7 +657,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // the peer no longer writes into this CTA or arrives on its barriers
   if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();

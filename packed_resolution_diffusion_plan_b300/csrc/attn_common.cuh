@@ -139,6 +139,100 @@ __device__ __forceinline__ float rope_row_to_f16(uint8_t* tile, int r, int2 p, c
   return amax;
 }
 
+// Part `part` of kParts of row r of a 128-row bf16 tile, rotated in place and
+// rounded to fp16 like rope_row_to_f16: the part takes the same share of both
+// halves (the first D/2 columns, which turn by the latent row, and the rest,
+// which turn by the column), so that kParts threads sharing a row do equal
+// work.  Rows at or past the sample's end (valid = false) become zero.
+// Returns the largest |value| written.
+template <int D, bool kScale, int kParts>
+__device__ __forceinline__ float rope_part_row_to_f16(uint8_t* tile, int r, int part, int2 p, bool valid,
+                                                      const float* rope_cs, const float* rope_hl, float mult) {
+  constexpr int nf = D / 4;
+  constexpr int kHalfChunks = D / 16;
+  constexpr int n = kHalfChunks / kParts;
+  static_assert(n * kParts == kHalfChunks, "parts must split a half into whole chunks");
+  const int k0 = part * n;
+  float amax = 0.f;
+  auto chunk_ptr = [&](int c16) {
+    return reinterpret_cast<uint4*>(tile + (c16 >> 3) * 16384 + sw128_off(r, c16 & 7));
+  };
+  auto finish = [&](uint32_t (&w)[4], const float (&y)[8]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float y0 = kScale ? y[2 * e] * mult : y[2 * e], y1 = kScale ? y[2 * e + 1] * mult : y[2 * e + 1];
+      amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+      w[e] = pack_f16(y0, y1);
+    }
+  };
+  if (!valid) {
+#pragma unroll
+    for (int k = 0; k < n; ++k) {
+      *chunk_ptr(k0 + k) = make_uint4(0, 0, 0, 0);
+      *chunk_ptr(kHalfChunks + k0 + k) = make_uint4(0, 0, 0, 0);
+    }
+    return 0.f;
+  }
+  if (p.x < 0) {  // text row: scale and round only
+#pragma unroll 2
+    for (int k = 0; k < 2 * n; ++k) {
+      uint4* ptr = chunk_ptr((k < n ? 0 : kHalfChunks - n) + k0 + k);
+      uint4 v = *ptr;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        y[2 * e] = bf16_lo(w[e]);
+        y[2 * e + 1] = bf16_hi(w[e]);
+      }
+      finish(*reinterpret_cast<uint32_t(*)[4]>(w), y);
+      *ptr = v;
+    }
+    return amax;
+  }
+  // first half: (cos, sin) of p.x from the full table
+  const float2* full = reinterpret_cast<const float2*>(rope_cs) + static_cast<size_t>(p.x) * nf;
+#pragma unroll 2
+  for (int k = k0; k < k0 + n; ++k) {
+    uint4* ptr = chunk_ptr(k);
+    uint4 v = *ptr;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 F = __ldg(full + 4 * k + e);
+      const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
+      y[2 * e] = fmaf(x0, F.x, -x1 * F.y);
+      y[2 * e + 1] = fmaf(x0, F.y, x1 * F.x);
+    }
+    finish(*reinterpret_cast<uint32_t(*)[4]>(w), y);
+    *ptr = v;
+  }
+  // second half: the two-level factors of p.y
+  const float2* hi = reinterpret_cast<const float2*>(rope_hl);  // [nf][32]
+  const float2* lo = hi + nf * 32;                              // [nf][32]
+  const int hc = p.y >> 5, lc = p.y & 31;
+#pragma unroll 2
+  for (int k = k0; k < k0 + n; ++k) {
+    uint4* ptr = chunk_ptr(kHalfChunks + k);
+    uint4 v = *ptr;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 A = __ldg(hi + (4 * k + e) * 32 + hc);
+      const float2 B = __ldg(lo + (4 * k + e) * 32 + lc);
+      const float c = fmaf(A.x, B.x, -A.y * B.y), s = fmaf(A.y, B.x, A.x * B.y);
+      const float x0 = bf16_lo(w[e]), x1 = bf16_hi(w[e]);
+      y[2 * e] = fmaf(x0, c, -x1 * s);
+      y[2 * e + 1] = fmaf(x0, s, x1 * c);
+    }
+    finish(*reinterpret_cast<uint32_t(*)[4]>(w), y);
+    *ptr = v;
+  }
+  return amax;
+}
+
 // The same rotation of row r with its 16-byte chunks software-pipelined:
 // chunk c + 1's row data and table entries are loaded before chunk c is
 // rotated and stored (the in-place store would otherwise order every later
