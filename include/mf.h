@@ -147,8 +147,9 @@ MF_API mf_status mf_attn_fwd(const void *q, const void *k, const void *v, const 
                       float *lse, void *stream);
 
 /* Bytes of device workspace mf_attn_bwd needs: float32 row dots
- * D = rowsum(dO * O) [heads, total_tokens] and a float32 dQ accumulator
- * [total_tokens, heads, head_dim]. */
+ * D = rowsum(dO * O) [heads, total_tokens], a float32 dQ accumulator
+ * [total_tokens, heads, head_dim] and fp16 rotated copies R(Q), s log2(e) R(K)
+ * of the same shape (each section 256-byte aligned). */
 MF_API mf_status mf_attn_bwd_workspace_size(int32_t total_tokens, int32_t heads, int32_t head_dim,
                                      size_t *bytes);
 
@@ -167,8 +168,8 @@ MF_API mf_status mf_attn_bwd(const void *q, const void *k, const void *v, const 
                       int32_t head_dim, float softmax_scale, void *workspace,
                       size_t workspace_bytes, void *dq, void *dk, void *dv, void *stream);
 
-/* Size of the fixed device scratch behind mf_attn_bwd_noalloc (64 MiB). */
-#define MF_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+/* Size of the fixed device scratch behind mf_attn_bwd_noalloc (128 MiB). */
+#define MF_NOALLOC_SCRATCH_BYTES (128u * 1024u * 1024u)
 
 /* mf_attn_bwd for callers that cannot allocate device memory.  (The Mage-Flow
  * pages have no counterpart: this is a deployment convenience of the

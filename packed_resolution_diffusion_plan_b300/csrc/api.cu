@@ -108,11 +108,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [rows, heads*head_dim] bf16 view of a [T, heads, head_dim] tensor; boxes of
-// box_rows (128 or 64) rows x 64 columns, 128-byte swizzle, zero fill past
+// [rows, heads*head_dim] view of a [T, heads, head_dim] tensor of 16-bit
+// elements; boxes of 128 rows x 64 columns, 128-byte swizzle, zero fill past
 // the last row.
-mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t heads, int32_t head_dim,
-                    uint32_t box_rows = mf::kTile) {
+mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t heads, int32_t head_dim) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     g_last_cuda_error = "cuTensorMapEncodeTiled entry point not available";
@@ -121,7 +120,7 @@ mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t he
   const cuuint64_t cols = static_cast<cuuint64_t>(heads) * head_dim;
   cuuint64_t gdim[2] = {cols, static_cast<cuuint64_t>(rows)};
   cuuint64_t gstride[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mf::kTile)};
   cuuint32_t estride[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
                    estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -293,7 +292,9 @@ mf_status mf_attn_bwd_workspace_size(int32_t total_tokens, int32_t heads, int32_
   if (bytes == nullptr || total_tokens < 0 || heads < 1) return MF_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
   const size_t rows = static_cast<size_t>(total_tokens) * heads;
-  *bytes = align_up(rows * sizeof(float), 256) + align_up(rows * head_dim * sizeof(float), 256);
+  // D | float32 dQ accumulator | fp16 q~ | fp16 k~
+  *bytes = align_up(rows * sizeof(float), 256) + align_up(rows * head_dim * sizeof(float), 256) +
+           2 * align_up(rows * head_dim * 2, 256);
   return MF_OK;
 }
 
@@ -312,24 +313,31 @@ mf_status mf_attn_bwd(const void* q, const void* k, const void* v, const void* o
   size_t need = 0;
   if ((st = mf_attn_bwd_workspace_size(plan->total_tokens, heads, head_dim, &need)) != MF_OK) return st;
   if (workspace_bytes < need) return MF_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv, tdo;
-  // Q is loaded in 64-row halves (each CTA of a cluster rotates one half).
-  if ((st = make_tmap(&tq, q, plan->total_tokens, heads, head_dim, 64)) != MF_OK) return st;
-  if ((st = make_tmap(&tk, k, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
-  if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
-  if ((st = make_tmap(&tdo, dout, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   const size_t rows = static_cast<size_t>(plan->total_tokens) * heads;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t off_acc = align_up(rows * sizeof(float), 256);
+  const size_t off_qr = off_acc + align_up(rows * head_dim * sizeof(float), 256);
+  const size_t off_kr = off_qr + align_up(rows * head_dim * 2, 256);
   mf::BwdArgs a;
   a.g = make_geom(plan, heads);
-  // clusters of two CTAs over pairs of K/V tiles (the forward's 256-row units)
-  a.g.n_items = 2 * plan->n_pairs * heads;
   a.scale = resolve_scale(softmax_scale, head_dim);
   a.scale_log2 = a.scale * kLog2e;
+  a.q = q;
+  a.k = k;
   a.o = o;
   a.dout = dout;
   a.lse = lse;
-  a.dsum = static_cast<float*>(workspace);
-  a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align_up(rows * sizeof(float), 256));
+  a.dsum = reinterpret_cast<float*>(ws);
+  a.dq_acc = reinterpret_cast<float*>(ws + off_acc);
+  a.q_rot = ws + off_qr;
+  a.k_rot = ws + off_kr;
+  // The main kernel streams the rotated fp16 copies that bwd_pre writes
+  // (16-bit elements: the tensor maps only move bytes).
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = make_tmap(&tq, a.q_rot, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tk, a.k_rot, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tdo, dout, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;

@@ -9,16 +9,12 @@
 //
 // Three kernels:
 //   bwd_pre      D = rowsum(dO * O) (float32 [heads, T]); zero the float32 dQ
-//                accumulator.
+//                accumulator; q~ = R(q) and k~ = s log2(e) R(k) as fp16
+//                [T, heads, D], rotated once per token.
 //   bwd_main     one CTA per (sample, head, 128-row K/V tile), streaming the
-//                sample's 128-row Q/dO tiles (a two-slot Q ring, one dO
-//                slot).  CTAs run in clusters of two over K/V tiles 2p and
-//                2p + 1, which stream the same Q tiles: each loads and rotates
-//                64 rows of every Q tile (a half row per RoPE thread) and
-//                stores them into both CTAs' shared memory, halving the
-//                rotation work per CTA.  Per Q
-//                tile i, five tcgen05 MMAs (TMEM columns: A = 0..127,
-//                B = 128..255, dV = 256.., dK = 256 + D..):
+//                sample's 128-row q~/dO tiles (a two-slot q~ ring, one dO
+//                slot).  Per Q tile i, five tcgen05 MMAs (TMEM columns:
+//                A = 0..127, B = 128..255, dV = 256.., dK = 256 + D..):
 //                  S^T_i  = k~ q~_i^T        fp16, smem x smem -> A
 //                  dP^T_i = V dO_i^T         bf16, smem x smem -> B
 //                  dV    += P^T_i dO_i       bf16, P^T from TMEM (A) x smem
@@ -29,57 +25,51 @@
 //                           into the staging tile cover one 128-byte row
 //                issued in the order dV_i, dK_i, dQ_i, S^T_{i+1}, dP^T_{i+1}:
 //                the compute warps move dQ_i out of B while S^T_{i+1} runs.
-//                16 warps:
+//                12 warps:
 //                  WG0, WG1  thread r owns K/V row r (TMEM lane r), WG c the
 //                            query columns 64c..64c+63: P^T = exp2(S^T - LSE2)
 //                            written back over its S^T columns as packed bf16,
 //                            dS^T = P^T * (dP^T - D) as fp16 into shared
 //                            memory; the dQ epilogue (TMEM -> staging tile,
 //                            half the tile each); at the end dV and R^T dk~
-//                  WG2       RoPE of the K tile (once, pre-scaled by
-//                            s * log2 e so S^T is in exp2 units) and of every
-//                            Q tile (fp16) from the plan's two-level table,
-//                            which stays in L1; per-tile LSE2 / D rows into
-//                            shared memory
-//                  WG3       warp 12 TMA producer (Q ring of two, one dO
-//                            slot), warp 13 TMEM owner and MMA issuer, warp
-//                            14 the dQ reducer: with head_dim 128 each half of
+//                  WG2       warp 8 TMA producer (q~ ring of two, one dO
+//                            slot), warp 9 TMEM owner and MMA issuer, warp
+//                            10 the dQ reducer: with head_dim 128 each half of
 //                            dQ_i is staged in shared memory by its compute
 //                            warpgroup and added into the float accumulator
 //                            by one TMA reduce, so the compute warps never
-//                            wait on the reduction traffic
+//                            wait on the reduction traffic; warp 11 the
+//                            per-tile -LSE2 / -D rows
 //   bwd_dq       dq = R^T (s * accumulator) as bf16.
 #include "attn_common.cuh"
 
 namespace mf {
 namespace {
 
-constexpr int kThreads = 16 * 32;
-constexpr int kRopeWG = 2;
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kReduceWarp = 14;
+constexpr int kThreads = 12 * 32;
+constexpr int kCtrlWG = 2;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kReduceWarp = 10;
+constexpr int kRowWarp = 11;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 // Per-thread register shares after setmaxnreg; they add up to the launch's
-// 4 x 128 per thread.
-constexpr uint32_t kRegsCompute = 184, kRegsRope = 72, kRegsCtrl = 72;
-constexpr int kRopeUnroll = 2;  // K tile rotation (once per CTA)
-static_assert(2 * kRegsCompute + kRegsRope + kRegsCtrl <= 4 * 128,
-              "warpgroup register shares exceed the launch's registers");
+// 3 x 168 per thread (65,536 / 384 rounded down to a multiple of 8).
+constexpr uint32_t kRegsCompute = 208, kRegsCtrl = 88;
+static_assert(2 * kRegsCompute + kRegsCtrl <= 3 * 168, "warpgroup register shares exceed the launch's registers");
 
 // Barriers and CTA-wide scalars of bwd_main, kept in dynamic shared memory
 // after the tiles (the kernel has no static shared memory, so the dynamic
 // base is the start of the CTA's window and the tiles stay 1024-aligned).
 struct BwdCtl {
-  uint64_t kv_full, k_ready, fin;
+  uint64_t kv_full, fin;
   uint64_t q_full[2], q_ready[2], q_free[2], do_full, do_free;
   uint64_t s_full, p_ready, dp_full, ds_ready, dv_done, dq_full, dq_free;
   uint64_t stage_full[2], stage_free[2];
   uint32_t tmem;
   int abort;
-  int range;
-  int pad;
+  int pad[3];
   WorkItem item;
 };
 
@@ -105,26 +95,65 @@ struct BwdCfg {
 
 // ---------------------------------------------------------------- bwd_pre
 // One thread per (token, head, 8-column chunk); a group of D/8 lanes reduces
-// one row.  Also zeroes the matching 8 accumulator floats.
+// one row of D.  The thread also zeroes the matching 8 accumulator floats and
+// writes the chunk of q~ = R(q) and of k~ = s log2(e) R(k) as fp16: the main
+// kernel streams every Q tile once per K/V tile of its sample, so rotating
+// here, once per token, replaces that many rotations of each tile.  A value
+// beyond the fp16 range (or a NaN) raises the range status.
 template <int D>
 __global__ void bwd_pre_kernel(const BwdArgs a) {
   constexpr int kChunks = D / 8;
+  constexpr int nf = D / 4;
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long rows = static_cast<long long>(a.g.total_tokens) * a.g.heads;
   const long long row = gid / kChunks;
   const int ch = static_cast<int>(gid % kChunks);
   float acc = 0.f;
   if (row < rows) {
-    const uint4 o = reinterpret_cast<const uint4*>(a.o)[row * kChunks + ch];
-    const uint4 g = reinterpret_cast<const uint4*>(a.dout)[row * kChunks + ch];
+    const long long tok = row / a.g.heads;
+    const uint4 o = reinterpret_cast<const uint4*>(a.o)[gid];
+    const uint4 g = reinterpret_cast<const uint4*>(a.dout)[gid];
+    const uint4 qv = reinterpret_cast<const uint4*>(a.q)[gid];
+    const uint4 kv = reinterpret_cast<const uint4*>(a.k)[gid];
     const uint32_t* ow = reinterpret_cast<const uint32_t*>(&o);
     const uint32_t* gw = reinterpret_cast<const uint32_t*>(&g);
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(&qv);
+    const uint32_t* kw = reinterpret_cast<const uint32_t*>(&kv);
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       acc += bf16_lo(ow[e]) * bf16_lo(gw[e]) + bf16_hi(ow[e]) * bf16_hi(gw[e]);
-    float4* z = reinterpret_cast<float4*>(a.dq_acc) + (row * kChunks + ch) * 2;
+    float4* z = reinterpret_cast<float4*>(a.dq_acc) + gid * 2;
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // (cos, sin) of the chunk's four pairs: the first D/2 columns turn by the
+    // latent row, the rest by the column; text tokens are not rotated.
+    const int2 p = reinterpret_cast<const int2*>(a.g.pos)[tok];
+    float cs[8] = {1.f, 0.f, 1.f, 0.f, 1.f, 0.f, 1.f, 0.f};
+    if (p.x >= 0) {
+      const int dim0 = ch * 8;
+      const int k0 = (dim0 % (D / 2)) / 2;
+      const int pp = dim0 >= D / 2 ? p.y : p.x;
+      const float4* tab = reinterpret_cast<const float4*>(a.g.rope_cs) + static_cast<size_t>(pp) * (nf / 2) + k0 / 2;
+      const float4 c0 = __ldg(tab), c1 = __ldg(tab + 1);
+      cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
+      cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
+    }
+    uint32_t qo[4], ko[4];
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float c = cs[2 * e], sn = cs[2 * e + 1];
+      const float q0 = bf16_lo(qw[e]), q1 = bf16_hi(qw[e]);
+      const float k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
+      const float yq0 = fmaf(q0, c, -q1 * sn), yq1 = fmaf(q0, sn, q1 * c);
+      const float yk0 = fmaf(k0, c, -k1 * sn) * a.scale_log2, yk1 = fmaf(k0, sn, k1 * c) * a.scale_log2;
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(yq0), fabsf(yq1)), fmaxf(fabsf(yk0), fabsf(yk1))));
+      qo[e] = pack_f16(yq0, yq1);
+      ko[e] = pack_f16(yk0, yk1);
+    }
+    reinterpret_cast<uint4*>(a.q_rot)[gid] = make_uint4(qo[0], qo[1], qo[2], qo[3]);
+    reinterpret_cast<uint4*>(a.k_rot)[gid] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+    if (!(amax <= kF16Max)) atomicOr(a.g.status, kStatusRange);
   }
 #pragma unroll
   for (int off = kChunks / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -208,7 +237,7 @@ __device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32
 }
 
 template <int D>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                 const __grid_constant__ CUtensorMap tdq, const BwdArgs args) {
@@ -225,18 +254,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   volatile int* abort_flag = &c.abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
-  // The two CTAs of a cluster own consecutive K/V tiles 2p and 2p + 1 of one
-  // (sample, head) and stream the same Q tiles: each loads and rotates half
-  // of every Q tile's rows and writes them into both CTAs' shared memory.
-  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   if (tid == 0) {
     mbar_init(&c.kv_full, 1);
-    mbar_init(&c.k_ready, kTile);
     mbar_init(&c.fin, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&c.q_full[s], 1);
-      mbar_init(&c.q_ready[s], kTile);  // this CTA's RoPE threads, plus the peer's half as tx bytes
-      mbar_init(&c.q_free[s], 2);           // both CTAs' MMAs are done with the slot
+      mbar_init(&c.q_ready[s], 32);  // the row warp's lanes
+      mbar_init(&c.q_free[s], 1);
       mbar_init(&c.stage_full[s], kTile);
       mbar_init(&c.stage_free[s], 1);
     }
@@ -250,8 +274,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     mbar_init(&c.dq_full, 1);
     mbar_init(&c.dq_free, 2 * kTile);
     c.abort = 0;
-    c.range = 0;
-    c.item = decode_item<2 * kTile>(args.g, blockIdx.x >> 1);  // tile = K/V tile pair
+    c.item = decode_item<kTile>(args.g, blockIdx.x);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -259,21 +282,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tmem_relinquish();
   }
   tc_fence_before();
-  cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrival
+  __syncthreads();
   tc_fence_after();
 
   const uint32_t tmem = c.tmem;
   const WorkItem w = c.item;
-  const int kv_tile = 2 * w.tile + static_cast<int>(rank);
-  // An odd tile count leaves the last pair's second CTA without rows: it
-  // still shares the Q rotation, and its K/V rows all count as invalid.
-  const int kv0 = w.seq_start + kv_tile * kTile;
-  const int kv_rows = max(0, min(kTile, w.len - kv_tile * kTile));
+  const int kv0 = w.seq_start + w.tile * kTile;
+  const int kv_rows = min(kTile, w.len - w.tile * kTile);
   const int n_q = (w.len + kTile - 1) / kTile;
   const int xcol = w.head * D;
   const int T = args.g.total_tokens;
 
-  if (wg == 3) {
+  if (wg == kCtrlWG) {
     regs_dec<kRegsCtrl>();
     if (warp == kProducerWarp && lane == 0) {
       tma_prefetch_desc(&tq);
@@ -291,11 +311,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const uint32_t ph_free = ((i >> 1) - 1) & 1;  // completion i/2 - 1 of the slot's free barrier
         const int y = w.seq_start + i * kTile;
         if (i >= 2 && !mbar_wait(&c.q_free[s], ph_free, abort_flag)) break;
-        // this CTA's 64 rows of Q_i (rank r: rows 64r ..); the peer writes the other half, rotated
-        mbar_arrive_expect_tx(&c.q_full[s], C::kTileBytes / 2);
+        mbar_arrive_expect_tx(&c.q_full[s], C::kTileBytes);
         for (int h = 0; h < C::kHalves; ++h)
-          tma_load_2d(smem + C::kOffQ + s * C::kTileBytes + h * 16384 + rank * 8192, &tq, &c.q_full[s], xcol + h * 64,
-                      y + 64 * static_cast<int>(rank));
+          tma_load_2d(smem + C::kOffQ + s * C::kTileBytes + h * 16384, &tq, &c.q_full[s], xcol + h * 64, y);
         nq_issued = i + 1;
         // dO_i reuses the one slot once dV_{i-1} has read dO_{i-1}.
         if (i >= 1 && !mbar_wait(&c.do_free, (i - 1) & 1, abort_flag)) break;
@@ -338,8 +356,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           mma_ss(tmem + C::kColB, kmaj(sV + off), kmaj(sDO + off), id_dp, kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(&c.k_ready, 0, abort_flag) && mbar_wait(&c.kv_full, 0, abort_flag) &&
-                mbar_wait(&c.q_ready[0], 0, abort_flag);
+      bool ok = mbar_wait(&c.kv_full, 0, abort_flag) && mbar_wait(&c.q_full[0], 0, abort_flag);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -373,7 +390,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_ss(tmem + C::kColDK, kmaj(sDS + off), mnmaj(sQ + s * C::kTileBytes + kk * 2048), id_dk, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit_multicast(&c.q_free[s], 0x3);  // frees the slot in both CTAs' accounting
+        mma_commit(&c.q_free[s]);
         // dQ_i into B (the compute warps have read dP^T_i before ds_ready).
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -388,7 +405,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         if (!more) break;
         // S^T_{i+1} into A (dV_i has read P^T_i out of it); it runs while the
         // compute warps move dQ_i out of B.
-        if (!mbar_wait(&c.q_ready[s1], ph1, abort_flag) || !mbar_wait(&c.dv_done, ph, abort_flag)) break;
+        if (!mbar_wait(&c.q_full[s1], ph1, abort_flag) || !mbar_wait(&c.dv_done, ph, abort_flag)) break;
         tc_fence_after();
         issue_s(s1);
         mma_commit(&c.s_full);
@@ -419,64 +436,25 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
       }
       bulk_wait_group0();
-    }
-  } else if (wg == kRopeWG) {
-    regs_dec<kRegsRope>();
-    const int r = tid - kRopeWG * 128;
-    const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
-    const float* tab_hl = args.g.rope_hl;
-    const float* tab_cs = args.g.rope_cs;
-    float amax = 0.f;
-    // fp16 q~ of row r of Q tile i, and that row's LSE2 / D.
-    // Threads 2j and 2j + 1 share row 64 * rank + j of each Q tile, each
-    // rotating the same share of both halves; the rotated rows are copied
-    // into the peer CTA's tile.
-    const int rr = 64 * static_cast<int>(rank) + (r >> 1), part = r & 1;
-    auto rope_q = [&](int i) -> bool {
-      const int s = i & 1;
-      const int q0 = w.seq_start + i * kTile;
-      const bool valid = r < w.len - i * kTile;
-      const bool valid_rr = rr < w.len - i * kTile;
-      const size_t idx = static_cast<size_t>(w.head) * T + q0 + r;
-      const int2 p = valid_rr ? pos[q0 + rr] : make_int2(-1, -1);
-      const float l2 = valid ? args.lse[idx] * kLog2e : INFINITY;  // invalid query: P = 0
-      const float dd = valid ? args.dsum[idx] : 0.f;
-      if (!warp_wait(&c.q_full[s], (i >> 1) & 1, abort_flag)) return false;
-      uint8_t* qt = smem + C::kOffQ + s * C::kTileBytes;
-      amax = fmaxf(amax, rope_part_row_to_f16<D, false, 2>(qt, rr, part, p, valid_rr, tab_cs, tab_hl, 1.0f));
-      // stored negated: P = exp2(S + (-LSE2)), dS = P * (dP + (-D)) on fp32 pairs
-      rowbuf[s * 2 * kTile + r] = -l2;
-      rowbuf[s * 2 * kTile + kTile + r] = -dd;
-      fence_proxy_async_smem();
-      // Once the whole half is rotated, one thread copies it into the peer's
-      // slot (the peer freed it: q_free counts both CTAs' MMAs), completing
-      // on the peer's q_ready as transaction bytes; this CTA's q_ready
-      // expects the peer's half the same way.
-      named_bar_sync(3, kTile);
-      if (r == 0) {
-        const uint32_t bar_peer = mapa_shared(smem_u32(&c.q_ready[s]), peer);
-        for (int h = 0; h < C::kHalves; ++h) {
-          uint8_t* src = qt + h * 16384 + rank * 8192;
-          bulk_copy_to_cluster(mapa_shared(smem_u32(src), peer), src, 8192, bar_peer);
+    } else if (warp == kRowWarp) {
+      // -LSE2 and -D of Q tile i's rows into the slot's row buffer, once the
+      // compute warps are done with tile i - 2 (its dK has completed).
+      // Queries past the sample's end get -LSE2 = -inf, hence P = 0.
+      for (int i = 0; i < n_q; ++i) {
+        const int s = i & 1;
+        if (i >= 2 && !warp_wait(&c.q_free[s], ((i >> 1) - 1) & 1, abort_flag)) break;
+        const int q0 = w.seq_start + i * kTile;
+#pragma unroll
+        for (int k = 0; k < kTile / 32; ++k) {
+          const int r = lane + 32 * k;
+          const bool valid = r < w.len - i * kTile;
+          const size_t idx = static_cast<size_t>(w.head) * T + q0 + r;
+          rowbuf[s * 2 * kTile + r] = valid ? -args.lse[idx] * kLog2e : -INFINITY;
+          rowbuf[s * 2 * kTile + kTile + r] = valid ? -args.dsum[idx] : 0.f;
         }
-        mbar_arrive_expect_tx(&c.q_ready[s], C::kTileBytes / 2);
-      } else {
         mbar_arrive(&c.q_ready[s]);
       }
-      return true;
-    };
-    bool ok = warp_wait(&c.kv_full, 0, abort_flag);
-    if (ok) {
-      uint8_t* kt = smem + C::kOffK;
-      if (r < kv_rows)
-        amax = fmaxf(amax, rope_row_to_f16<D, true, kRopeUnroll>(kt, r, pos[kv0 + r], tab_cs, tab_hl, args.scale_log2));
-      else zero_row<D>(kt, r);
-      fence_proxy_async_smem();
-      mbar_arrive(&c.k_ready);
-      ok = rope_q(0);
     }
-    for (int i = 1; ok && i < n_q; ++i) ok = rope_q(i);
-    if (!(amax <= kF16Max)) c.range = 1;
   } else {
     regs_inc<kRegsCompute>();
     // Thread r owns K/V row r (TMEM lane r); warpgroup cw the query columns
@@ -657,14 +635,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   }
 
   tc_fence_before();
-  cluster_sync_all();  // the peer no longer writes into this CTA or arrives on its barriers
+  __syncthreads();
   if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (tid == 0 && (c.abort || c.range))
-    atomicOr(args.g.status, (c.abort ? kStatusTimeout : 0) | (c.range ? kStatusRange : 0));
+  if (tid == 0 && c.abort) atomicOr(args.g.status, kStatusTimeout);
 }
 
 template <int D>

@@ -75,10 +75,14 @@ struct BwdArgs {
   AttnGeom g;
   float scale;               // softmax_scale
   float scale_log2;          // softmax_scale * log2(e)
+  const void* q;             // bf16 [T, heads, D]
+  const void* k;
   const void* o;
   const void* dout;
   const float* lse;
   float* dsum;               // [heads, T] rowsum(dO * O)
+  void* q_rot;               // fp16 [T, heads, D] q~ = R(q)
+  void* k_rot;               // fp16 [T, heads, D] k~ = s log2(e) R(k)
   float* dq_acc;             // [T, heads, D] float32 accumulator (zeroed by the preprocess)
   void* dq;
   void* dk;

@@ -1,13 +1,13 @@
 // mf_attn_bwd_noalloc: the attention backward for callers that cannot
 // allocate device memory.
 //
-// mf_attn_bwd needs a scratch workspace (the float32 row dots D and the
-// float32 dQ accumulator) that the caller normally allocates.  Some callers
-// cannot allocate at the point where they run the backward: for example an
-// engine plugin whose execute step is forbidden to allocate, a runtime that
-// hands all device memory to its own pool at start-up and has none left to
-// give, or a latency-critical loop that must not call cudaMalloc because it
-// can synchronize the device.  For them this file keeps a fixed scratch
+// mf_attn_bwd needs a scratch workspace (the float32 row dots D, the float32
+// dQ accumulator and fp16 rotated copies of Q and K) that the caller normally
+// allocates.  Some callers cannot allocate at the point where they run the
+// backward: for example an engine plugin whose execute step is forbidden to
+// allocate, a runtime that hands all device memory to its own pool at
+// start-up and has none left to give, or a latency-critical loop that must
+// not call cudaMalloc because it can synchronize the device.  For them this file keeps a fixed scratch
 // array in device memory, reserved when the library's GPU code is loaded and
 // held by every GPU that loads it until the process exits.
 #include <atomic>
@@ -57,8 +57,9 @@ extern "C" mf_status mf_attn_bwd_noalloc(const void* q, const void* k, const voi
   if (need > kScratchBytes) return MF_ERR_UNSUPPORTED;  // pack too large for the fixed scratch
   void* scratch = nullptr;
   if ((st = scratch_address(&scratch)) != MF_OK) return st;
-  // The backward's first kernel overwrites D and zeroes the accumulator, so
-  // whatever an earlier call left in the array does not leak into this one.
+  // The backward's first kernel overwrites D and the rotated copies and zeroes
+  // the accumulator, so whatever an earlier call left in the array does not
+  // leak into this one.
   return mf_attn_bwd(q, k, v, o, lse, dout, plan, heads, head_dim, softmax_scale, scratch, kScratchBytes, dq,
                      dk, dv, stream);
 }

@@ -53,7 +53,7 @@ def test_noalloc_matches_workspace_backward_two_calls_in_a_row():
     fn = _noalloc_fn()
     cases = [
         ([(0, 16, 16), (7, 64, 32), (0, 128, 128), (200, 160, 48), (55, 96, 208)], 3, 128, 1),
-        (synth.single_1024().samples, 24, 128, 2),  # 4224 tokens: 52 MB of scratch
+        (synth.single_1024().samples, 24, 128, 2),  # 4224 tokens: 104 MB of scratch
     ]
     for samples, heads, head_dim, seed in cases:
         plan, q, k, v, do, o, lse = _case(samples, heads, head_dim, seed)
@@ -66,7 +66,7 @@ def test_noalloc_matches_workspace_backward_two_calls_in_a_row():
 
 def test_noalloc_rejects_packs_beyond_the_scratch():
     fn = _noalloc_fn()
-    plan = mf.pack_plan(synth.native_res(0).samples, token_budget=32768)   # ~400 MB of scratch
+    plan = mf.pack_plan(synth.native_res(0).samples, token_budget=32768)   # ~800 MB of scratch
     z = ctypes.c_void_p(1 << 20)
     st = fn(z, z, z, z, z, z, ctypes.byref(plan.raw), 24, 128, 0.0, z, z, z, None)
     assert mf.STATUS[st] == "MF_ERR_UNSUPPORTED"
