@@ -238,13 +238,14 @@ def run_mf(args):
     lse = torch.empty((H, T), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     ws = torch.empty(mf.bwd_workspace_bytes(T, H, D), dtype=torch.uint8, device=dev)
+    ws_fwd = torch.empty(mf.fwd_workspace_bytes(T, H, D), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
         plan = mf.pack_plan(wl.samples, token_budget=wl.token_budget, head_dim=D, device=dev)
         if ev is not None:
             mf.record_main_kernel(ev[0], ev[1])
-        mf.attn_fwd(q, k, v, plan, out=o, lse=lse)
+        mf.attn_fwd(q, k, v, plan, out=o, lse=lse, workspace=ws_fwd)
         if ev is not None:
             mf.record_main_kernel(ev[2], ev[3])
         mf.attn_bwd(q, k, v, o, lse, do, plan, workspace=ws, dq=dq, dk=dk, dv=dv)
@@ -253,7 +254,7 @@ def run_mf(args):
     for _ in range(max(args.warmup, 1)):
         plan = step()
     mf.check(plan)
-    launches_per_step = 3 + 1 + 3  # scan, ids, RoPE table; forward; bwd pre, main, dq
+    launches_per_step = 3 + 2 + 3  # scan, ids, RoPE table; fwd pre, main; bwd pre, main, dq
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

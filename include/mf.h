@@ -134,17 +134,28 @@ MF_API mf_status mf_pack_plan(const mf_sample *samples, int32_t n_samples, int32
                        int32_t head_dim, float rope_theta, void *workspace,
                        size_t workspace_bytes, mf_plan *plan_out, void *stream);
 
+/* Bytes of device workspace mf_attn_fwd needs: fp16 rotated copies
+ * s log2(e) R(Q) and R(K) [total_tokens, heads, head_dim] (each section
+ * 256-byte aligned). */
+MF_API mf_status mf_attn_fwd_workspace_size(int32_t total_tokens, int32_t heads, int32_t head_dim,
+                                            size_t *bytes);
+
 /* Forward: for every sample i and head h,
  *   O = softmax(s * R(Q) R(K)^T) V,  LSE = logsumexp(s * R(Q) R(K)^T)  (rows)
  * over that sample's tokens only, R = the 2D rotation above.
- *   q, k, v   device bf16 [plan->total_tokens, heads, head_dim]
- *   o         device bf16, same shape (written)
- *   lse       device float32 [heads, plan->total_tokens] (written)
+ *   q, k, v     device bf16 [plan->total_tokens, heads, head_dim]
+ *   workspace   device memory of mf_attn_fwd_workspace_size bytes, 256-byte
+ *               aligned (contents on entry are ignored; a first kernel writes
+ *               the rotated copies that the attention kernel streams)
+ *   o           device bf16, same shape (written)
+ *   lse         device float32 [heads, plan->total_tokens] (written)
  * Errors: MF_ERR_INVALID_ARG (null/misaligned pointer, heads < 1, head_dim
- * different from the plan's), MF_ERR_UNSUPPORTED, MF_ERR_CUDA. */
+ * different from the plan's, short workspace), MF_ERR_UNSUPPORTED,
+ * MF_ERR_CUDA.  A rotated value beyond the fp16 range shows up as
+ * MF_ERR_RANGE from mf_check. */
 MF_API mf_status mf_attn_fwd(const void *q, const void *k, const void *v, const mf_plan *plan,
-                      int32_t heads, int32_t head_dim, float softmax_scale, void *o,
-                      float *lse, void *stream);
+                      int32_t heads, int32_t head_dim, float softmax_scale, void *workspace,
+                      size_t workspace_bytes, void *o, float *lse, void *stream);
 
 /* Bytes of device workspace mf_attn_bwd needs: float32 row dots
  * D = rowsum(dO * O) [heads, total_tokens], a float32 dQ accumulator

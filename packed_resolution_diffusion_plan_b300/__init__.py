@@ -26,7 +26,7 @@ library_path = os.path.join(_HERE, "libmf.so")
 STATUS = {0: "MF_OK", 1: "MF_ERR_INVALID_ARG", 2: "MF_ERR_UNSUPPORTED", 3: "MF_ERR_BUDGET",
           4: "MF_ERR_CUDA", 5: "MF_ERR_TIMEOUT", 6: "MF_ERR_RANGE"}
 
-EXPORTED_SYMBOLS = ["mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd",
+EXPORTED_SYMBOLS = ["mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd_workspace_size", "mf_attn_fwd",
                     "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_attn_bwd_noalloc", "mf_check",
                     "mf_record_main_kernel",
                     "mf_status_string", "mf_last_cuda_error"]
@@ -75,8 +75,9 @@ def lib():
                                               ctypes.POINTER(c_sz)]
     L.mf_pack_plan.argtypes = [ctypes.POINTER(MfSample), c_i32, c_i32, c_i32, ctypes.c_float, c_vp,
                                c_sz, ctypes.POINTER(MfPlan), c_vp]
+    L.mf_attn_fwd_workspace_size.argtypes = [c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]
     L.mf_attn_fwd.argtypes = [c_vp, c_vp, c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32, ctypes.c_float,
-                              c_vp, c_vp, c_vp]
+                              c_vp, c_sz, c_vp, c_vp, c_vp]
     L.mf_attn_bwd_workspace_size.argtypes = [c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]
     L.mf_attn_bwd.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32,
                               ctypes.c_float, c_vp, c_sz, c_vp, c_vp, c_vp, c_vp]
@@ -86,7 +87,7 @@ def lib():
     L.mf_status_string.restype = ctypes.c_char_p
     L.mf_last_cuda_error.argtypes = []
     L.mf_last_cuda_error.restype = ctypes.c_char_p
-    for name in ("mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd",
+    for name in ("mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd_workspace_size", "mf_attn_fwd",
                  "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_record_main_kernel"):
         getattr(L, name).restype = c_i32
     _lib = L
@@ -184,7 +185,15 @@ def _check_qkv(plan: Plan, *ts):
             raise ValueError("shape mismatch")
 
 
-def attn_fwd(q, k, v, plan: Plan, softmax_scale: float = 0.0, out=None, lse=None, stream=None):
+def fwd_workspace_bytes(total_tokens: int, heads: int, head_dim: int) -> int:
+    n = ctypes.c_size_t(0)
+    _raise(lib().mf_attn_fwd_workspace_size(total_tokens, heads, head_dim, ctypes.byref(n)),
+           "mf_attn_fwd_workspace_size")
+    return n.value
+
+
+def attn_fwd(q, k, v, plan: Plan, softmax_scale: float = 0.0, out=None, lse=None, workspace=None,
+             stream=None):
     """O, LSE of packed 2D-RoPE joint attention (see mf_attn_fwd)."""
     _check_qkv(plan, q, k, v)
     T, H, D = q.shape
@@ -192,9 +201,12 @@ def attn_fwd(q, k, v, plan: Plan, softmax_scale: float = 0.0, out=None, lse=None
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(256, fwd_workspace_bytes(T, H, D)), dtype=torch.uint8, device=q.device)
     _raise(lib().mf_attn_fwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
                              ctypes.c_void_p(v.data_ptr()), ctypes.byref(plan.raw), H, D,
-                             float(softmax_scale), ctypes.c_void_p(out.data_ptr()),
+                             float(softmax_scale), ctypes.c_void_p(workspace.data_ptr()),
+                             workspace.numel(), ctypes.c_void_p(out.data_ptr()),
                              ctypes.c_void_p(lse.data_ptr()), _stream_ptr(stream, q.device)),
            "mf_attn_fwd")
     return out, lse

@@ -263,24 +263,45 @@ mf_status mf_pack_plan(const mf_sample* samples, int32_t n_samples, int32_t toke
   return MF_OK;
 }
 
+mf_status mf_attn_fwd_workspace_size(int32_t total_tokens, int32_t heads, int32_t head_dim, size_t* bytes) {
+  if (bytes == nullptr || total_tokens < 0 || heads < 1) return MF_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
+  const size_t rows = static_cast<size_t>(total_tokens) * heads;
+  // fp16 q~ | fp16 k~
+  *bytes = 2 * align_up(rows * head_dim * 2, 256);
+  return MF_OK;
+}
+
 mf_status mf_attn_fwd(const void* q, const void* k, const void* v, const mf_plan* plan, int32_t heads,
-                      int32_t head_dim, float softmax_scale, void* o, float* lse, void* stream) {
+                      int32_t head_dim, float softmax_scale, void* workspace, size_t workspace_bytes, void* o,
+                      float* lse, void* stream) {
   mf_status st = check_attn_common(plan, heads, head_dim);
   if (st != MF_OK) return st;
   if (plan->total_tokens == 0) return MF_OK;
-  if (!q || !k || !v || !o || !lse) return MF_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse || !workspace) return MF_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return MF_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv;
-  if ((st = make_tmap(&tq, q, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
-  if ((st = make_tmap(&tk, k, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
-  if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MF_ERR_INVALID_ARG;
+  size_t need = 0;
+  if ((st = mf_attn_fwd_workspace_size(plan->total_tokens, heads, head_dim, &need)) != MF_OK) return st;
+  if (workspace_bytes < need) return MF_ERR_INVALID_ARG;
+  const size_t rows = static_cast<size_t>(plan->total_tokens) * heads;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
   mf::FwdArgs a;
   a.g = make_geom(plan, heads);
   a.g.n_items = plan->n_pairs * heads;  // the forward works on 256-row tile pairs
   a.scale_log2 = resolve_scale(softmax_scale, head_dim) * kLog2e;
+  a.q = q;
+  a.k = k;
+  a.q_rot = ws;
+  a.k_rot = ws + align_up(rows * head_dim * 2, 256);
   a.o = o;
   a.lse = lse;
+  // The main kernel streams the rotated fp16 copies that fwd_pre writes.
+  CUtensorMap tq, tk, tv;
+  if ((st = make_tmap(&tq, a.q_rot, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tk, a.k_rot, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   cudaEvent_t ev0, ev1;
   take_events(&ev0, &ev1);
   cudaError_t e = mf::launch_attn_fwd(a, tq, tk, tv, head_dim, static_cast<cudaStream_t>(stream), ev0, ev1);

@@ -6,30 +6,35 @@
 // tokens, confined to each sample by cumulative offsets; Hugging Face paper
 // page, Highlights "System-level speed": per-sample 2D RoPE).
 //
-// One CTA owns a pair of 128-row Q tiles (256 query rows) of one (sample,
-// head) and streams the sample's 128-row K/V tiles, so every K tile it
-// rotates serves 256 query rows.  16 warps in four warpgroups:
-//   WG0, WG1   softmax of Q tile 0 / 1: thread t owns query row t (TMEM lane
-//              t); online softmax in the exp2 domain, O rescaled in TMEM only
-//              when the running max grows by more than 2^8; P written back
-//              into its S columns of TMEM as packed bf16; epilogue O / l, LSE
-//   WG2        RoPE: rotates the Q tiles once and each landed K tile (one row
-//              per thread) in shared memory, so no rotated copy reaches HBM.
-//              Rotated rows are stored as fp16 (Q pre-multiplied by
-//              softmax_scale * log2 e): the logit MMA runs fp16 x fp16 -> fp32,
-//              whose 11-bit significand keeps the rotation's rounding 8x below
-//              bf16's, and S lands in TMEM already in exp2 units
-//   WG3        warp 12: TMA producer (Q pair once; K into a 3-slot ring freed
-//              right after both logit MMAs, V into a 2-slot ring); warp 13:
-//              TMEM owner and single-thread MMA issuer:
-//                S_a = Q_a K_j^T (smem x smem), O_a += P_a V_j (P from TMEM),
-//              in the ping-pong order QK_0(j), PV_1(j-1), QK_1(j), PV_0(j),
-//              so one tile's softmax overlaps the other tile's MMAs
+// Two kernels:
+//   fwd_pre    q~ = s log2(e) R(q) and k~ = R(k) as fp16 [T, heads, D], once per
+//              token (the main kernel streams each K tile once per Q-tile pair
+//              of its sample, so rotating there repeated the work that many
+//              times).  fp16 keeps the rotation's rounding 8x below bf16's,
+//              and with s log2(e) folded into q~ the logits land in TMEM
+//              already in exp2 units.  A value beyond the fp16 range raises
+//              the range status.
+//   attn_fwd   one CTA owns a pair of 128-row Q tiles (256 query rows) of one
+//              (sample, head) and streams the sample's 128-row k~/V tiles.
+//              12 warps in three warpgroups:
+//     WG0, WG1   softmax of Q tile 0 / 1: thread t owns query row t (TMEM
+//                lane t); online softmax in the exp2 domain, O rescaled in
+//                TMEM only when the running max grows by more than 2^8; P
+//                written back into its S columns of TMEM as packed bf16;
+//                epilogue O / l, LSE
+//     WG2        warp 8: TMA producer (the q~ pair once; k~ into a 3-slot ring
+//                freed right after both logit MMAs, V into a 2-slot ring);
+//                warp 9: TMEM owner and single-thread MMA issuer:
+//                  S_a = q~_a k~_j^T (smem x smem), O_a += P_a V_j (P from
+//                  TMEM), in the ping-pong order QK_0(j), PV_1(j-1), QK_1(j),
+//                  PV_0(j), so one tile's softmax overlaps the other tile's
+//                  MMAs
 // TMEM: S0 | S1 | O0 | O1 (128 + 128 + D + D columns of 512).  Registers are
-// rebalanced with setmaxnreg (the four warpgroup shares sum to the launch's
-// 4 x 128 per thread).
-// Rows past the sample's end: K/Q rows are zeroed after rotation, S columns
-// past the end are masked to -inf, Q rows past the end are never stored.
+// rebalanced with setmaxnreg (the warpgroup shares sum to the launch's
+// 3 x 168 per thread).
+// Rows past the sample's end: S columns past the end are masked to -inf
+// (their P is exactly 0, so the V rows they meet add nothing), and Q rows
+// past the end are never stored.
 #include "attn_common.cuh"
 
 namespace mf {
@@ -51,18 +56,62 @@ struct FwdCfg {
   static constexpr uint32_t kTmemCols = 512;
 };
 
-constexpr int kThreads = 16 * 32;
-constexpr int kRopeWG = 2;
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
+constexpr int kThreads = 12 * 32;
+constexpr int kCtrlWG = 2;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kRopeUnroll = 2;
-// Per-thread register shares after setmaxnreg (chosen from ptxas spill
-// reports: the producer/MMA warpgroup needs ~80, RoPE ~72-80).
-constexpr uint32_t kRegsSoftmax = 168, kRegsRope = 104, kRegsCtrl = 72;
-static_assert(2 * kRegsSoftmax + kRegsRope + kRegsCtrl <= 4 * 128,
-              "warpgroup register shares exceed the launch's registers");
+// Per-thread register shares after setmaxnreg; they add up to the launch's
+// 3 x 168 per thread (65,536 / 384 rounded down to a multiple of 8).
+constexpr uint32_t kRegsSoftmax = 208, kRegsCtrl = 88;
+static_assert(2 * kRegsSoftmax + kRegsCtrl <= 3 * 168, "warpgroup register shares exceed the launch's registers");
+
+// ---------------------------------------------------------------- fwd_pre
+// One thread per (token, head, 8-column chunk): the chunk's four rotation
+// pairs of q and k (the first D/2 columns turn by the latent row, the rest by
+// the column; text tokens are not rotated), rounded to fp16.
+template <int D>
+__global__ void fwd_pre_kernel(const FwdArgs a) {
+  constexpr int kChunks = D / 8;
+  constexpr int nf = D / 4;
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long rows = static_cast<long long>(a.g.total_tokens) * a.g.heads;
+  if (gid >= rows * kChunks) return;
+  const long long tok = gid / kChunks / a.g.heads;
+  const int ch = static_cast<int>(gid % kChunks);
+  const uint4 qv = reinterpret_cast<const uint4*>(a.q)[gid];
+  const uint4 kv = reinterpret_cast<const uint4*>(a.k)[gid];
+  const uint32_t* qw = reinterpret_cast<const uint32_t*>(&qv);
+  const uint32_t* kw = reinterpret_cast<const uint32_t*>(&kv);
+  const int2 p = reinterpret_cast<const int2*>(a.g.pos)[tok];
+  float cs[8] = {1.f, 0.f, 1.f, 0.f, 1.f, 0.f, 1.f, 0.f};
+  if (p.x >= 0) {
+    const int dim0 = ch * 8;
+    const int k0 = (dim0 % (D / 2)) / 2;
+    const int pp = dim0 >= D / 2 ? p.y : p.x;
+    const float4* tab = reinterpret_cast<const float4*>(a.g.rope_cs) + static_cast<size_t>(pp) * (nf / 2) + k0 / 2;
+    const float4 c0 = __ldg(tab), c1 = __ldg(tab + 1);
+    cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
+    cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
+  }
+  uint32_t qo[4], ko[4];
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float c = cs[2 * e], sn = cs[2 * e + 1];
+    const float q0 = bf16_lo(qw[e]), q1 = bf16_hi(qw[e]);
+    const float k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
+    const float yq0 = fmaf(q0, c, -q1 * sn) * a.scale_log2, yq1 = fmaf(q0, sn, q1 * c) * a.scale_log2;
+    const float yk0 = fmaf(k0, c, -k1 * sn), yk1 = fmaf(k0, sn, k1 * c);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(yq0), fabsf(yq1)), fmaxf(fabsf(yk0), fabsf(yk1))));
+    qo[e] = pack_f16(yq0, yq1);
+    ko[e] = pack_f16(yk0, yk1);
+  }
+  reinterpret_cast<uint4*>(a.q_rot)[gid] = make_uint4(qo[0], qo[1], qo[2], qo[3]);
+  reinterpret_cast<uint4*>(a.k_rot)[gid] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+  if (!(amax <= kF16Max)) atomicOr(a.g.status, kStatusRange);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -71,22 +120,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_q_full, bar_q_ready, bar_final;
-  __shared__ uint64_t bar_k_full[C::kKStages], bar_k_rot[C::kKStages], bar_k_free[C::kKStages];
+  __shared__ uint64_t bar_q_full, bar_final;
+  __shared__ uint64_t bar_k_full[C::kKStages], bar_k_free[C::kKStages];
   __shared__ uint64_t bar_v_full[C::kVStages], bar_v_free[C::kVStages];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2];
   __shared__ uint32_t s_tmem;
-  __shared__ int s_abort, s_range;
+  __shared__ int s_abort;
   __shared__ WorkItem s_item;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
   if (tid == 0) {
     mbar_init(&bar_q_full, 1);
-    mbar_init(&bar_q_ready, kTile);
     mbar_init(&bar_final, 1);
     for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&bar_k_full[i], 1);
-      mbar_init(&bar_k_rot[i], kTile);
       mbar_init(&bar_k_free[i], 1);
     }
     for (int i = 0; i < C::kVStages; ++i) {
@@ -99,7 +146,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       mbar_init(&bar_pv_done[i], 1);
     }
     s_abort = 0;
-    s_range = 0;
     s_item = decode_item<2 * kTile>(args.g, blockIdx.x);
     fence_mbar_init();
   }
@@ -118,7 +164,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   const int n_kv = (w.len + kTile - 1) / kTile;
   const int xcol = w.head * D;
 
-  if (wg == 3) {
+  if (wg == kCtrlWG) {
     regs_dec<kRegsCtrl>();
     if (warp == kProducerWarp && lane == 0) {
       tma_prefetch_desc(&tq);
@@ -188,7 +234,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       // each tile's softmax overlaps the other tile's MMAs, and the two
       // softmaxes never run at the same time.  S_a holds P_a until PV_a has
       // read it, so QK_a waits for the tile's previous PV_a.
-      bool ok = mbar_wait(&bar_q_ready, 0, &s_abort) && mbar_wait(&bar_k_rot[0], 0, &s_abort);
+      bool ok = mbar_wait(&bar_q_full, 0, &s_abort) && mbar_wait(&bar_k_full[0], 0, &s_abort);
       if (ok) {
         tc_fence_after();
         issue_qk(0, 0);
@@ -212,7 +258,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tc_fence_after();
         issue_pv(0, j);
         if (j + 1 < n_kv) {
-          if (!mbar_wait(&bar_k_rot[(j + 1) % C::kKStages], ((j + 1) / C::kKStages) & 1, &s_abort) ||
+          if (!mbar_wait(&bar_k_full[(j + 1) % C::kKStages], ((j + 1) / C::kKStages) & 1, &s_abort) ||
               !mbar_wait(&bar_pv_done[0], j & 1, &s_abort)) {
             ok = false;
             break;
@@ -229,43 +275,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       mma_commit(&bar_final);
       wait_drain(&bar_final, 0);
     }
-  } else if (wg == kRopeWG) {
-    regs_dec<kRegsRope>();
-    // Thread r prepares row r of each tile for the logit MMA: fp16 of
-    // R(pos) q * scale * log2(e) for Q, fp16 of R(pos) k for K; rows past the
-    // sample's end are zeroed.
-    const int r = tid - kRopeWG * 128;
-    const int2* pos = reinterpret_cast<const int2*>(args.g.pos);
-    const float* tab_hl = args.g.rope_hl;
-    const float* tab_cs = args.g.rope_cs;
-    float amax = 0.f;
-    int2 pq[2];
-#pragma unroll
-    for (int a = 0; a < 2; ++a) pq[a] = (a * kTile + r < rows_left) ? pos[q0 + a * kTile + r] : make_int2(-1, -1);
-    if (mbar_wait(&bar_q_full, 0, &s_abort)) {
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        uint8_t* qt = smem + C::kOffQ + a * C::kTileBytes;
-        if (a * kTile + r < rows_left) amax = fmaxf(amax, rope_row_to_f16<D, true>(qt, r, pq[a], tab_cs, tab_hl, args.scale_log2));
-        else zero_row<D>(qt, r);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bar_q_ready);
-      int2 pk = (r < w.len) ? pos[w.seq_start + r] : make_int2(-1, -1);
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % C::kKStages;
-        const int kr = j * kTile + r;
-        // next tile's position, loaded while this one is in flight
-        const int2 pk_next = (kr + kTile < w.len) ? pos[w.seq_start + kr + kTile] : make_int2(-1, -1);
-        if (!mbar_wait(&bar_k_full[s], (j / C::kKStages) & 1, &s_abort)) break;
-        uint8_t* kt = smem + C::kOffK + s * C::kTileBytes;
-        amax = fmaxf(amax, rope_row_to_f16_pipelined<D, false>(kt, r, pk, kr < w.len, tab_cs, tab_hl, 1.0f));
-        fence_proxy_async_smem();
-        mbar_arrive(&bar_k_rot[s]);
-        pk = pk_next;
-      }
-    }
-    if (!(amax <= kF16Max)) s_range = 1;
   } else {
     regs_inc<kRegsSoftmax>();
     // Softmax warpgroup `a`: thread `row` owns query row `row` of Q tile a.
@@ -386,15 +395,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (tid == 0 && (s_abort || s_range))
-    atomicOr(args.g.status, (s_abort ? kStatusTimeout : 0) | (s_range ? kStatusRange : 0));
+  if (tid == 0 && s_abort) atomicOr(args.g.status, kStatusTimeout);
 }
 
 template <int D>
 cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
   using C = FwdCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
+  const long long chunks = static_cast<long long>(a.g.total_tokens) * a.g.heads * (D / 8);
+  fwd_pre_kernel<D><<<static_cast<unsigned>((chunks + 255) / 256), 256, 0, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return e;
   attn_fwd_kernel<D><<<a.g.n_items, kThreads, C::kDynSmem, stream>>>(tq, tk, tv, a);

@@ -62,6 +62,10 @@ struct AttnGeom {
 struct FwdArgs {
   AttnGeom g;
   float scale_log2;          // softmax_scale * log2(e), folded into the fp16 Q operand
+  const void* q;             // bf16 [T, heads, D]
+  const void* k;
+  void* q_rot;               // fp16 [T, heads, D] s log2(e) R(q)
+  void* k_rot;               // fp16 [T, heads, D] R(k)
   void* o;                   // bf16 [T, heads, D]
   float* lse;                // [heads, T]
 };

@@ -84,13 +84,22 @@ def test_attn_validation_without_gpu(L):
         setattr(plan, p, 4096)
     vp = ctypes.c_void_p
     ok = vp(1 << 20)
-    # null plan, bad heads, unsupported / mismatched head_dim, null or misaligned tensors
-    assert L.mf_attn_fwd(ok, ok, ok, None, 2, 128, 0.0, ok, ok, None) == 1
-    assert L.mf_attn_fwd(ok, ok, ok, ctypes.byref(plan), 0, 128, 0.0, ok, ok, None) == 1
-    assert L.mf_attn_fwd(ok, ok, ok, ctypes.byref(plan), 2, 96, 0.0, ok, ok, None) == 2
-    assert L.mf_attn_fwd(ok, ok, ok, ctypes.byref(plan), 2, 64, 0.0, ok, ok, None) == 1
-    assert L.mf_attn_fwd(None, ok, ok, ctypes.byref(plan), 2, 128, 0.0, ok, ok, None) == 1
-    assert L.mf_attn_fwd(vp((1 << 20) + 2), ok, ok, ctypes.byref(plan), 2, 128, 0.0, ok, ok, None) == 1
+    # null plan, bad heads, unsupported / mismatched head_dim, null or misaligned
+    # tensors, null / short / misaligned workspace
+    big = 1 << 30
+    assert L.mf_attn_fwd(ok, ok, ok, None, 2, 128, 0.0, ok, big, ok, ok, None) == 1
+    assert L.mf_attn_fwd(ok, ok, ok, ctypes.byref(plan), 0, 128, 0.0, ok, big, ok, ok, None) == 1
+    assert L.mf_attn_fwd(ok, ok, ok, ctypes.byref(plan), 2, 96, 0.0, ok, big, ok, ok, None) == 2
+    assert L.mf_attn_fwd(ok, ok, ok, ctypes.byref(plan), 2, 64, 0.0, ok, big, ok, ok, None) == 1
+    assert L.mf_attn_fwd(None, ok, ok, ctypes.byref(plan), 2, 128, 0.0, ok, big, ok, ok, None) == 1
+    assert L.mf_attn_fwd(vp((1 << 20) + 2), ok, ok, ctypes.byref(plan), 2, 128, 0.0, ok, big, ok, ok, None) == 1
+    assert L.mf_attn_fwd(ok, ok, ok, ctypes.byref(plan), 2, 128, 0.0, None, big, ok, ok, None) == 1
+    assert L.mf_attn_fwd(ok, ok, ok, ctypes.byref(plan), 2, 128, 0.0, ok, 16, ok, ok, None) == 1
+    assert L.mf_attn_fwd(ok, ok, ok, ctypes.byref(plan), 2, 128, 0.0, vp((1 << 20) + 16), big, ok, ok, None) == 1
+    n = ctypes.c_size_t(0)
+    assert L.mf_attn_fwd_workspace_size(10, 2, 128, ctypes.byref(n)) == 0
+    assert n.value >= 2 * 10 * 2 * 128 * 2
+    assert L.mf_attn_fwd_workspace_size(10, 2, 96, ctypes.byref(n)) == 2
     assert L.mf_attn_bwd(ok, ok, ok, ok, ok, ok, ctypes.byref(plan), 2, 128, 0.0, ok, 16,
                          ok, ok, ok, None) == 1
     assert L.mf_attn_bwd(ok, ok, ok, ok, ok, None, ctypes.byref(plan), 2, 128, 0.0, ok, 1 << 30,
@@ -102,5 +111,5 @@ def test_attn_validation_without_gpu(L):
     # an empty pack is a no-op that needs no tensors
     empty = mf.MfPlan()
     empty.head_dim = 128
-    assert L.mf_attn_fwd(None, None, None, ctypes.byref(empty), 2, 128, 0.0, None, None, None) == 0
+    assert L.mf_attn_fwd(None, None, None, ctypes.byref(empty), 2, 128, 0.0, None, 0, None, None, None) == 0
     assert L.mf_check(None, None) == 1
