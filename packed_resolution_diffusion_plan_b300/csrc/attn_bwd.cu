@@ -65,7 +65,7 @@ static_assert(2 * kRegsCompute + kRegsCtrl <= 3 * 168, "warpgroup register share
 struct BwdCtl {
   uint64_t kv_full, fin;
   uint64_t q_full[2], q_ready[2], q_free[2], do_full, do_free;
-  uint64_t s_full, p_ready, dp_full, ds_ready, dv_done, dq_full, dq_free;
+  uint64_t s_full, p_ready, dp_full, ds_ready, a_free, dq_full, dq_free;
   uint64_t stage_full[2], stage_free[2];
   uint32_t tmem;
   int abort;
@@ -270,7 +270,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     mbar_init(&c.p_ready, 2 * kTile);
     mbar_init(&c.dp_full, 1);
     mbar_init(&c.ds_ready, 2 * kTile);
-    mbar_init(&c.dv_done, 1);
+    mbar_init(&c.a_free, 1);
     mbar_init(&c.dq_full, 1);
     mbar_init(&c.dq_free, 2 * kTile);
     c.abort = 0;
@@ -380,16 +380,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(tmem + C::kColDV, tmem + C::kColA + 64 * (kk >> 2) + 8 * (kk & 3),
                  mnmaj(sDO + kk * 2048), id_dv, (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&c.dv_done);
         mma_commit(&c.do_free);
-        // dk~ += dS^T_i q~_i
+        // dk~ += dS^T_i q~_i, with dS^T packed in the A columns beside P^T
+        // (query 64c.. at column 64c + 32).
         if (!mbar_wait(&c.ds_ready, ph, abort_flag)) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDK, kmaj(sDS + off), mnmaj(sQ + s * C::kTileBytes + kk * 2048), id_dk, (i > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + C::kColDK, tmem + C::kColA + 32 + 64 * (kk >> 2) + 8 * (kk & 3),
+                 mnmaj(sQ + s * C::kTileBytes + kk * 2048), id_dk, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&c.a_free);  // dV_i and dK_i have read P^T and dS^T out of A
         mma_commit(&c.q_free[s]);
         // dQ_i into B (the compute warps have read dP^T_i before ds_ready).
 #pragma unroll
@@ -403,9 +403,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         mma_commit(&c.dq_full);
         if (!more) break;
-        // S^T_{i+1} into A (dV_i has read P^T_i out of it); it runs while the
-        // compute warps move dQ_i out of B.
-        if (!mbar_wait(&c.q_full[s1], ph1, abort_flag) || !mbar_wait(&c.dv_done, ph, abort_flag)) break;
+        // S^T_{i+1} into A (dV_i and dK_i have read P^T_i and dS^T_i out of
+        // it); it runs while the compute warps move dQ_i out of B.
+        if (!mbar_wait(&c.q_full[s1], ph1, abort_flag) || !mbar_wait(&c.a_free, ph, abort_flag)) break;
         tc_fence_after();
         issue_s(s1);
         mma_commit(&c.s_full);
@@ -594,11 +594,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
           for (int j = 0; j < 16; ++j) dw[j] = 0u;
         }
+        // dS^T: packed fp16 into the dead S^T columns of A (the dK operand)
+        // and into shared memory (the dQ operand)
+        tmem_st16(tl + C::kColA + 64 * cw + 32 + 16 * hh, dw);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
           *reinterpret_cast<uint4*>(dst_ds + sw128_off(r, 4 * hh + ch)) =
               make_uint4(dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&c.ds_ready);
