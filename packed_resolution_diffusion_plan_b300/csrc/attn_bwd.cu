@@ -36,10 +36,12 @@
 //                            slot), warp 9 TMEM owner and MMA issuer, warp
 //                            10 the dQ reducer: with head_dim 128 each half of
 //                            dQ_i is staged in shared memory by its compute
-//                            warpgroup and added into the float accumulator
-//                            by one TMA reduce, so the compute warps never
-//                            wait on the reduction traffic; warp 11 the
-//                            per-tile -LSE2 / -D rows
+//                            warpgroup (one in the staging tile, one in the
+//                            q~_i slot, idle from dK_i until the producer
+//                            refills it) and added into the float
+//                            accumulator by one TMA reduce, so the compute
+//                            warps never wait on the reduction traffic; warp
+//                            11 the per-tile -LSE2 / -D rows
 //   bwd_dq       dq = R^T (s * accumulator) as bf16.
 #include "attn_common.cuh"
 
@@ -66,7 +68,7 @@ struct BwdCtl {
   uint64_t kv_full, fin;
   uint64_t q_full[2], q_ready[2], q_free[2], do_full, do_free;
   uint64_t s_full, p_ready, dp_full, ds_ready, a_free, dq_full, dq_free;
-  uint64_t stage_full[2], stage_free[2];
+  uint64_t stage_full[2], stage_free;
   uint32_t tmem;
   int abort;
   int pad[3];
@@ -260,9 +262,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     for (int s = 0; s < 2; ++s) {
       mbar_init(&c.q_full[s], 1);
       mbar_init(&c.q_ready[s], 32);  // the row warp's lanes
-      mbar_init(&c.q_free[s], 1);
+      // head_dim 128: dK_i has read the slot, and the reducer has read the
+      // dQ_i half staged in it
+      mbar_init(&c.q_free[s], D == 128 ? 2 : 1);
       mbar_init(&c.stage_full[s], kTile);
-      mbar_init(&c.stage_free[s], 1);
     }
     mbar_init(&c.do_full, 1);
     mbar_init(&c.do_free, 1);
@@ -273,6 +276,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     mbar_init(&c.a_free, 1);
     mbar_init(&c.dq_full, 1);
     mbar_init(&c.dq_free, 2 * kTile);
+    mbar_init(&c.stage_free, 1);
     c.abort = 0;
     c.item = decode_item<kTile>(args.g, blockIdx.x);
     fence_mbar_init();
@@ -419,21 +423,22 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       wait_drain(&c.fin, 0);
     } else if (D == 128 && warp == kReduceWarp && lane == 0) {
       // Reducer: each staged half of dQ_i (64 queries x D floats) is added
-      // into the accumulator by one TMA reduce; once the TMA has read it the
-      // other compute warpgroup may stage its half.
+      // into the accumulator by one TMA reduce.  Warpgroup 0's half sits in
+      // the staging tile, warpgroup 1's in the q~_i slot (free once dK_i has
+      // read it, and handed back to the producer once the reduce has read it).
       tma_prefetch_desc(&tdq);
-      bool ok = true;
-      for (int i = 0; ok && i < n_q; ++i) {
-        for (int cw = 0; cw < 2; ++cw) {
-          if (!mbar_wait(&c.stage_full[cw], i & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tma_reduce_add_3d(&tdq, smem + C::kOffStage, 0, w.head, w.seq_start + i * kTile + 64 * cw);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(&c.stage_free[1 - cw]);
-        }
+      for (int i = 0; i < n_q; ++i) {
+        const int y = w.seq_start + i * kTile;
+        if (!mbar_wait(&c.stage_full[0], i & 1, abort_flag)) break;
+        tma_reduce_add_3d(&tdq, smem + C::kOffStage, 0, w.head, y);
+        bulk_commit_group();
+        if (!mbar_wait(&c.stage_full[1], i & 1, abort_flag)) break;
+        tma_reduce_add_3d(&tdq, smem + C::kOffQ + (i & 1) * C::kTileBytes, 0, w.head, y + 64);
+        bulk_commit_group();
+        bulk_wait_group_read<1>();
+        mbar_arrive(&c.stage_free);
+        bulk_wait_group_read0();
+        mbar_arrive(&c.q_free[i & 1]);
       }
       bulk_wait_group0();
     } else if (warp == kRowWarp) {
@@ -466,10 +471,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     uint8_t* dst_ds = smem + C::kOffDS + cw * 16384;
     // dQ of Q tile i (TMEM B) into the float accumulator; warpgroup cw takes
     // half of it (queries 64cw ..) and releases B to the next dP^T as soon as
-    // its loads land.  With head_dim 128 the half is staged in shared memory
-    // (float [64 queries][D], TMEM lane r = dimension r) for the reducer's
-    // TMA reduce-add: warpgroup 0 stages right away, warpgroup 1 after the
-    // exponentials of the next tile, once the TMA has read warpgroup 0's half.
+    // its loads land.  With head_dim 128 both halves are staged in shared
+    // memory right away (float [64 queries][D], TMEM lane r = dimension r)
+    // for the reducer's TMA reduce-adds: warpgroup 0's in the staging tile,
+    // warpgroup 1's in the q~_i slot, which dK_i has finished with.
     float dqv[64];
     auto dq_load = [&](int i) -> bool {
       if (!warp_wait(&c.dq_full, i & 1, abort_flag)) return false;
@@ -509,10 +514,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     };
     auto dq_stage = [&](int i) -> bool {
       if (D != 128) return true;
-      if (cw == 0 ? (i >= 1 && !warp_wait(&c.stage_free[0], (i - 1) & 1, abort_flag))
-                  : !warp_wait(&c.stage_free[1], i & 1, abort_flag))
-        return false;
-      float* st = reinterpret_cast<float*>(smem + C::kOffStage) + r;
+      if (cw == 0 && i >= 1 && !warp_wait(&c.stage_free, (i - 1) & 1, abort_flag)) return false;
+      float* st = reinterpret_cast<float*>(smem + (cw == 0 ? C::kOffStage : C::kOffQ + (i & 1) * C::kTileBytes)) + r;
 #pragma unroll
       for (int j = 0; j < 64; ++j) st[j * D] = dqv[j];
       fence_proxy_async_smem();
@@ -522,7 +525,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       const int s = i & 1;
-      if (i > 0 && (!dq_load(i - 1) || (cw == 0 && !dq_stage(i - 1)))) {
+      if (i > 0 && (!dq_load(i - 1) || !dq_stage(i - 1))) {
         ok = false;
         break;
       }
@@ -562,7 +565,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&c.p_ready);
-      if (i > 0 && cw == 1 && !dq_stage(i - 1)) { ok = false; break; }
       if (!warp_wait(&c.dp_full, i & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
