@@ -423,22 +423,23 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       wait_drain(&c.fin, 0);
     } else if (D == 128 && warp == kReduceWarp && lane == 0) {
       // Reducer: each staged half of dQ_i (64 queries x D floats) is added
-      // into the accumulator by one TMA reduce.  Warpgroup 0's half sits in
-      // the staging tile, warpgroup 1's in the q~_i slot (free once dK_i has
-      // read it, and handed back to the producer once the reduce has read it).
+      // into the accumulator by one TMA reduce.  Warpgroup 1's half sits in
+      // the q~_i slot (free once dK_i has read it) and goes first, so that
+      // the slot returns to the producer early enough to land q~_{i+2} before
+      // it is needed; warpgroup 0's half sits in the staging tile.
       tma_prefetch_desc(&tdq);
       for (int i = 0; i < n_q; ++i) {
         const int y = w.seq_start + i * kTile;
-        if (!mbar_wait(&c.stage_full[0], i & 1, abort_flag)) break;
-        tma_reduce_add_3d(&tdq, smem + C::kOffStage, 0, w.head, y);
-        bulk_commit_group();
         if (!mbar_wait(&c.stage_full[1], i & 1, abort_flag)) break;
         tma_reduce_add_3d(&tdq, smem + C::kOffQ + (i & 1) * C::kTileBytes, 0, w.head, y + 64);
         bulk_commit_group();
+        if (!mbar_wait(&c.stage_full[0], i & 1, abort_flag)) break;
+        tma_reduce_add_3d(&tdq, smem + C::kOffStage, 0, w.head, y);
+        bulk_commit_group();
         bulk_wait_group_read<1>();
-        mbar_arrive(&c.stage_free);
-        bulk_wait_group_read0();
         mbar_arrive(&c.q_free[i & 1]);
+        bulk_wait_group_read0();
+        mbar_arrive(&c.stage_free);
       }
       bulk_wait_group0();
     } else if (warp == kRowWarp) {
