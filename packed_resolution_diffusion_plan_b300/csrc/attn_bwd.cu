@@ -68,7 +68,7 @@ struct BwdCtl {
   uint64_t kv_full, fin;
   uint64_t q_full[2], q_ready[2], q_free[2], do_full, do_free;
   uint64_t s_full, p_ready, dp_full, ds_ready, a_free, dq_full, dq_free;
-  uint64_t stage_full[2], stage_free;
+  uint64_t stage_full[2], stage_free, q_issued;
   uint32_t tmem;
   int abort;
   int pad[3];
@@ -277,6 +277,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     mbar_init(&c.dq_full, 1);
     mbar_init(&c.dq_free, 2 * kTile);
     mbar_init(&c.stage_free, 1);
+    mbar_init(&c.q_issued, 1);
     c.abort = 0;
     c.item = decode_item<kTile>(args.g, blockIdx.x);
     fence_mbar_init();
@@ -318,6 +319,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         mbar_arrive_expect_tx(&c.q_full[s], C::kTileBytes);
         for (int h = 0; h < C::kHalves; ++h)
           tma_load_2d(smem + C::kOffQ + s * C::kTileBytes + h * 16384, &tq, &c.q_full[s], xcol + h * 64, y);
+        if (i >= 2) mbar_arrive(&c.q_issued);  // the refill of the slot is in the TMA queue
         nq_issued = i + 1;
         // dO_i reuses the one slot once dV_{i-1} has read dO_{i-1}.
         if (i >= 1 && !mbar_wait(&c.do_free, (i - 1) & 1, abort_flag)) break;
@@ -424,20 +426,23 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     } else if (D == 128 && warp == kReduceWarp && lane == 0) {
       // Reducer: each staged half of dQ_i (64 queries x D floats) is added
       // into the accumulator by one TMA reduce.  Warpgroup 1's half sits in
-      // the q~_i slot (free once dK_i has read it) and goes first, so that
-      // the slot returns to the producer early enough to land q~_{i+2} before
-      // it is needed; warpgroup 0's half sits in the staging tile.
+      // the q~_i slot (free once dK_i has read it) and goes first; once the
+      // TMA has read it the slot returns to the producer, and warpgroup 0's
+      // half (in the staging tile) is issued only after the refill of the
+      // slot, so that the TMA unit, which takes its work in order, does not
+      // hold the q~_{i+2} load behind a second reduce.
       tma_prefetch_desc(&tdq);
       for (int i = 0; i < n_q; ++i) {
         const int y = w.seq_start + i * kTile;
         if (!mbar_wait(&c.stage_full[1], i & 1, abort_flag)) break;
         tma_reduce_add_3d(&tdq, smem + C::kOffQ + (i & 1) * C::kTileBytes, 0, w.head, y + 64);
         bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(&c.q_free[i & 1]);
+        if (i + 2 < n_q && !mbar_wait(&c.q_issued, i & 1, abort_flag)) break;
         if (!mbar_wait(&c.stage_full[0], i & 1, abort_flag)) break;
         tma_reduce_add_3d(&tdq, smem + C::kOffStage, 0, w.head, y);
         bulk_commit_group();
-        bulk_wait_group_read<1>();
-        mbar_arrive(&c.q_free[i & 1]);
         bulk_wait_group_read0();
         mbar_arrive(&c.stage_free);
       }
