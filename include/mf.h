@@ -101,10 +101,6 @@ typedef struct {
   int32_t *cu_seqlens;  /* device int32 [n_samples + 1], exclusive scan of L_i */
   int32_t *pos;         /* device int32 [total_tokens][2]: (row, col); text = (-1, -1) */
   float *rope_cs;       /* device float32 [max_grid][head_dim/4][2]: cos, sin of p*f_i */
-  float *rope_hl;       /* device float32 [2][head_dim/4][32][2]: cos, sin of (32 h) f_i
-                           (part 0, index h) and of l f_i (part 1, index l), h, l < 32; the
-                           attention kernels rotate position p = 32 h + l by the product of
-                           the two, from 16 KB of table that stays in the L1 cache */
   int32_t *order;       /* device int32 [n_samples][4]: (sample, first tile, first tile pair, 0),
                            longest sample first */
   int32_t *status;      /* device int32 status word written by kernels that time out */

@@ -44,7 +44,7 @@ class MfPlan(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
                 ("n_pairs", ctypes.c_int32),
                 ("cu_seqlens", ctypes.c_void_p), ("pos", ctypes.c_void_p),
-                ("rope_cs", ctypes.c_void_p), ("rope_hl", ctypes.c_void_p), ("order", ctypes.c_void_p),
+                ("rope_cs", ctypes.c_void_p), ("order", ctypes.c_void_p),
                 ("status", ctypes.c_void_p)]
 
 
@@ -148,11 +148,6 @@ class Plan:
     def rope_table(self) -> torch.Tensor:
         n = self.max_grid * (self.head_dim // 4) * 2
         return self._view(self.raw.rope_cs, n, torch.float32).view(self.max_grid, self.head_dim // 4, 2)
-
-    def rope_table_hl(self) -> torch.Tensor:
-        """The two-level table: [2, head_dim/4, 32, 2] (cos, sin) of (32 j) f_i and of j f_i."""
-        n = 2 * (self.head_dim // 4) * 32 * 2
-        return self._view(self.raw.rope_hl, n, torch.float32).view(2, self.head_dim // 4, 32, 2)
 
     def order(self) -> torch.Tensor:
         return self._view(self.raw.order, 4 * self.n_samples, torch.int32).view(-1, 4)

@@ -38,7 +38,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // ---------------------------------------------------------------- plan
 struct PlanLayout {
-  size_t off_scalars, off_samples, off_cu, off_order, off_pos, off_rope, off_hl, bytes;
+  size_t off_scalars, off_samples, off_cu, off_order, off_pos, off_rope, bytes;
   int32_t token_bound, grid_bound;
 };
 
@@ -83,8 +83,6 @@ mf_status check_samples(const mf_sample* samples, int32_t n, int32_t budget, int
   off = align_up(off + static_cast<size_t>(L->token_bound) * 2 * sizeof(int32_t), 256);
   L->off_rope = off;
   off = align_up(off + static_cast<size_t>(gmax) * (head_dim / 4) * 2 * sizeof(float), 256);
-  L->off_hl = off;
-  off = align_up(off + static_cast<size_t>(2 * 32) * (head_dim / 4) * 2 * sizeof(float), 256);
   L->bytes = off;
   return MF_OK;
 }
@@ -165,7 +163,7 @@ mf_status check_attn_common(const mf_plan* plan, int32_t heads, int32_t head_dim
   if (head_dim != plan->head_dim) return MF_ERR_INVALID_ARG;
   if (plan->total_tokens < 0 || plan->n_samples < 0) return MF_ERR_INVALID_ARG;
   if (plan->total_tokens > 0 &&
-      (plan->cu_seqlens == nullptr || plan->pos == nullptr || plan->rope_cs == nullptr || plan->rope_hl == nullptr ||
+      (plan->cu_seqlens == nullptr || plan->pos == nullptr || plan->rope_cs == nullptr ||
        plan->order == nullptr || plan->status == nullptr))
     return MF_ERR_INVALID_ARG;
   if (static_cast<long long>(plan->n_tiles) * heads >= (1ll << 31)) return MF_ERR_UNSUPPORTED;
@@ -178,7 +176,6 @@ mf::AttnGeom make_geom(const mf_plan* plan, int32_t heads) {
   g.cu_seqlens = plan->cu_seqlens;
   g.pos = plan->pos;
   g.rope_cs = plan->rope_cs;
-  g.rope_hl = plan->rope_hl;
   g.order = plan->order;
   g.n_samples = plan->n_samples;
   g.total_tokens = plan->total_tokens;
@@ -230,7 +227,6 @@ mf_status mf_pack_plan(const mf_sample* samples, int32_t n_samples, int32_t toke
   a.pos = reinterpret_cast<int32_t*>(ws + L.off_pos);
   a.token_bound = L.token_bound;
   a.rope_cs = reinterpret_cast<float*>(ws + L.off_rope);
-  a.rope_hl = reinterpret_cast<float*>(ws + L.off_hl);
   a.grid_bound = L.grid_bound;
   a.head_dim = head_dim;
   a.theta = rope_theta;
@@ -257,7 +253,6 @@ mf_status mf_pack_plan(const mf_sample* samples, int32_t n_samples, int32_t toke
   plan_out->cu_seqlens = a.cu_seqlens;
   plan_out->pos = a.pos;
   plan_out->rope_cs = a.rope_cs;
-  plan_out->rope_hl = a.rope_hl;
   plan_out->order = a.order;
   plan_out->status = &a.scalars->status;
   return MF_OK;

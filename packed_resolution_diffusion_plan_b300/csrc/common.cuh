@@ -34,7 +34,6 @@ struct PlanArgs {
   int32_t* pos;             // [token_bound][2]
   int32_t token_bound;
   float* rope_cs;           // [grid_bound][head_dim/4][2]
-  float* rope_hl;           // [2][head_dim/4][32][2]: e^{i 32h f_k}, e^{i l f_k}
   int32_t grid_bound;
   int32_t head_dim;
   float theta;
@@ -50,7 +49,6 @@ struct AttnGeom {
   const int32_t* cu_seqlens;
   const int32_t* pos;
   const float* rope_cs;
-  const float* rope_hl;
   const int32_t* order;
   int32_t n_samples;
   int32_t total_tokens;

@@ -163,30 +163,17 @@ __global__ void pack_pos_kernel(PlanArgs a) {
 }
 
 // cos/sin(p * f_i), f_i = theta^(-2i/(head_dim/2)), i < head_dim/4, for
-// p < grid_bound ([p][i] order), followed by the two-level table ([part][i][j]
-// order): part 0 at angle (32 j) f_i, part 1 at angle j f_i, j < 32.  Angles
-// and sin/cos are evaluated in double and rounded to float once.
+// p < grid_bound ([p][i] order).  Angles and sin/cos are evaluated in double
+// and rounded to float once.
 __global__ void rope_table_kernel(PlanArgs a) {
   const int nf = a.head_dim / 4;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  const int n_full = a.grid_bound * nf;
-  if (idx >= n_full + 64 * nf) return;
-  int i, p;
-  if (idx < n_full) {
-    p = idx / nf;
-    i = idx % nf;
-  } else {
-    const int h = idx - n_full;  // [part][i][j]
-    const int part = h / (32 * nf);
-    i = (h / 32) % nf;
-    p = part == 0 ? 32 * (h % 32) : h % 32;
-  }
+  if (idx >= a.grid_bound * nf) return;
+  const int p = idx / nf, i = idx % nf;
   const double f = pow(static_cast<double>(a.theta), -2.0 * i / (a.head_dim / 2));
   double sv, cv;
   sincos(static_cast<double>(p) * f, &sv, &cv);
-  const float2 v = make_float2(static_cast<float>(cv), static_cast<float>(sv));
-  if (idx < n_full) reinterpret_cast<float2*>(a.rope_cs)[idx] = v;
-  else reinterpret_cast<float2*>(a.rope_hl)[idx - n_full] = v;
+  reinterpret_cast<float2*>(a.rope_cs)[idx] = make_float2(static_cast<float>(cv), static_cast<float>(sv));
 }
 
 }  // namespace
@@ -200,7 +187,7 @@ cudaError_t launch_pack_plan(const PlanArgs& a, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int nt = (a.grid_bound + 64) * (a.head_dim / 4);
+  const int nt = a.grid_bound * (a.head_dim / 4);
   if (a.grid_bound > 0) {
     rope_table_kernel<<<(nt + 255) / 256, 256, 0, stream>>>(a);
     e = cudaGetLastError();

@@ -80,7 +80,7 @@ def test_plan_validation_without_gpu(L):
 def test_attn_validation_without_gpu(L):
     plan = mf.MfPlan()
     plan.total_tokens, plan.n_samples, plan.head_dim, plan.n_tiles = 10, 1, 128, 1
-    for p in ("cu_seqlens", "pos", "rope_cs", "rope_hl", "order", "status"):
+    for p in ("cu_seqlens", "pos", "rope_cs", "order", "status"):
         setattr(plan, p, 4096)
     vp = ctypes.c_void_p
     ok = vp(1 << 20)

@@ -43,19 +43,6 @@ def _check_plan(samples, budget, head_dim=128, theta=10000.0):
         ang = np.arange(p.max_grid)[:, None] * f[None, :]
         assert np.abs(tab[..., 0] - np.cos(ang)).max() < 1e-7
         assert np.abs(tab[..., 1] - np.sin(ang)).max() < 1e-7
-        # two-level table: part 0 at (32 j) f_i, part 1 at j f_i, [part][i][j]
-        hl = p.rope_table_hl().cpu().numpy().astype(np.float64)
-        j = np.arange(32)
-        for part, mult in ((0, 32), (1, 1)):
-            a2 = f[:, None] * (mult * j)[None, :]
-            assert np.abs(hl[part, ..., 0] - np.cos(a2)).max() < 1e-7
-            assert np.abs(hl[part, ..., 1] - np.sin(a2)).max() < 1e-7
-        # their product reproduces every position's rotation
-        pp = np.arange(p.max_grid)
-        A, B = hl[0][:, pp // 32], hl[1][:, pp % 32]          # [i, p, 2]
-        c = A[..., 0] * B[..., 0] - A[..., 1] * B[..., 1]
-        s = A[..., 1] * B[..., 0] + A[..., 0] * B[..., 1]
-        assert np.abs(c.T - np.cos(ang)).max() < 4e-7 and np.abs(s.T - np.sin(ang)).max() < 4e-7
     return p
 
 
