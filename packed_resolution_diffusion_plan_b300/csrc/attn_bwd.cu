@@ -319,7 +319,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         mbar_arrive_expect_tx(&c.q_full[s], C::kTileBytes);
         for (int h = 0; h < C::kHalves; ++h)
           tma_load_2d(smem + C::kOffQ + s * C::kTileBytes + h * 16384, &tq, &c.q_full[s], xcol + h * 64, y);
-        if (i >= 2) mbar_arrive(&c.q_issued);  // the refill of the slot is in the TMA queue
         nq_issued = i + 1;
         // dO_i reuses the one slot once dV_{i-1} has read dO_{i-1}.
         if (i >= 1 && !mbar_wait(&c.do_free, (i - 1) & 1, abort_flag)) break;
@@ -327,6 +326,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         for (int h = 0; h < C::kHalves; ++h)
           tma_load_2d(smem + C::kOffDO + h * 16384, &tdo, &c.do_full, xcol + h * 64, y);
         ndo_issued = i + 1;
+        if (i >= 2) mbar_arrive(&c.q_issued);  // the refill of the slot and dO_i are in the TMA queue
       }
       // Let this CTA's own copies land before its shared memory is released.
       wait_drain(&c.kv_full, 0);
@@ -429,8 +429,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       // the q~_i slot (free once dK_i has read it) and goes first; once the
       // TMA has read it the slot returns to the producer, and warpgroup 0's
       // half (in the staging tile) is issued only after the refill of the
-      // slot, so that the TMA unit, which takes its work in order, does not
-      // hold the q~_{i+2} load behind a second reduce.
+      // slot and the next dO load, so that the TMA unit, which takes its work
+      // in order, does not hold those loads behind a second reduce.
       tma_prefetch_desc(&tdq);
       for (int i = 0; i < n_q; ++i) {
         const int y = w.seq_start + i * kTile;
