@@ -176,6 +176,30 @@ def oracle_sample(wl, seconds, max_heads=None):
 
 
 # --------------------------------------------------------------------------
+# multi-rank host logic (N > 1 under torchrun; tested with gloo on CPU)
+# --------------------------------------------------------------------------
+
+def rank_workload(wl, rank):
+    """Rank `rank`'s pack: the same shapes as `wl`, its own tensor values."""
+    return synth.Workload(wl.name, wl.samples, wl.heads, wl.head_dim, wl.passes, wl.token_budget,
+                          wl.cfg_pairs, seed=wl.seed + 1000 * rank)
+
+
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest `x` over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, step_flop, ms_step):
+    """Whole-job throughput: every rank's step FLOPs over the slowest rank's time."""
+    return world * step_flop / (ms_step * 1e-3) / 1e12
+
+
+# --------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # --------------------------------------------------------------------------
 
@@ -229,9 +253,7 @@ def run_mf(args):
     wl = synth.WORKLOADS[args.workload](args.seed)
     fwd_flop, bwd_flop, lens = pack_flops(wl.samples, wl.heads, wl.head_dim)
     step_flop = fwd_flop + bwd_flop
-    wl_vals = synth.Workload(wl.name, wl.samples, wl.heads, wl.head_dim, wl.passes, wl.token_budget,
-                             wl.cfg_pairs, seed=args.seed + 1000 * rank)
-    host = synth.draw_tensors(wl_vals, with_grad=True)
+    host = synth.draw_tensors(rank_workload(wl, rank), with_grad=True)
     T, H, D = host["q"].shape
     q, k, v, do = (host[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
@@ -275,11 +297,8 @@ def run_mf(args):
     ms_step = t_start.elapsed_time(t_end) / args.steps
     fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     bwd_main_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
-    if dist:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * step_flop / (ms_step * 1e-3) / 1e12
+    ms_step = max_over_ranks(ms_step, dist, dev)
+    value = job_tflops(world, step_flop, ms_step)
 
     # ---- end to end through the public API with host buffers
     pin = {n: host[n].pin_memory() for n in ("q", "k", "v", "do")}
@@ -307,10 +326,7 @@ def run_mf(args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     mf.check(plan)
 
     if rank != 0:
@@ -354,7 +370,7 @@ def run_mf(args):
         "tokens_per_s": world * T / (ms_step * 1e-3),
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * step_flop / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+        "e2e": {"value": job_tflops(world, step_flop, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
