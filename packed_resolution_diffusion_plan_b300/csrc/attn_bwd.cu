@@ -478,9 +478,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     // dQ of Q tile i (TMEM B) into the float accumulator; warpgroup cw takes
     // half of it (queries 64cw ..) and releases B to the next dP^T as soon as
     // its loads land.  With head_dim 128 both halves are staged in shared
-    // memory right away (float [64 queries][D], TMEM lane r = dimension r)
-    // for the reducer's TMA reduce-adds: warpgroup 0's in the staging tile,
-    // warpgroup 1's in the q~_i slot, which dK_i has finished with.
+    // memory (float [64 queries][D], TMEM lane r = dimension r) for the
+    // reducer's TMA reduce-adds: warpgroup 0's in the staging tile after its
+    // next dS, warpgroup 1's right away in the q~_i slot, which dK_i has
+    // finished with.
     float dqv[64];
     auto dq_load = [&](int i) -> bool {
       if (!warp_wait(&c.dq_full, i & 1, abort_flag)) return false;
@@ -531,7 +532,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       const int s = i & 1;
-      if (i > 0 && (!dq_load(i - 1) || !dq_stage(i - 1))) {
+      // Warpgroup 1 stages dQ_{i-1} right away (its half frees a q~ slot);
+      // warpgroup 0 keeps its half in registers until after its dS, so that
+      // its exponentials never wait for the staging tile to drain.
+      if (i > 0 && (!dq_load(i - 1) || (cw == 1 && !dq_stage(i - 1)))) {
         ok = false;
         break;
       }
@@ -614,6 +618,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&c.ds_ready);
+      if (i > 0 && cw == 0 && !dq_stage(i - 1)) { ok = false; break; }
     }
     if (ok) ok = dq_load(n_q - 1) && dq_stage(n_q - 1);
     if (ok && warp_wait(&c.fin, 0, abort_flag)) {
