@@ -218,6 +218,20 @@ MF_API mf_status mf_check(const mf_plan *plan, void *stream);
  * exactly one of the two is NULL. */
 MF_API mf_status mf_record_main_kernel(void *start_event, void *stop_event);
 
+/* Test aid for the timeout path (the Mage-Flow pages have no counterpart).
+ * While `flags` is set, the attention calls made by this thread launch their
+ * main kernel with the TMA producer dropping its streamed-tile loads:
+ *   MF_DEBUG_DROP_FWD_KV   mf_attn_fwd issues no K/V tile loads,
+ *   MF_DEBUG_DROP_BWD_QDO  mf_attn_bwd issues no q~/dO tile loads,
+ * so the consumers' bounded waits run out (about 4 s), every warp leaves its
+ * loop, the kernel frees its TMEM and exits, and mf_check reports
+ * MF_ERR_TIMEOUT.  Nothing faults or hangs and the CUDA context stays usable.
+ * The outputs of such a call are undefined.  0 restores normal operation.
+ * MF_ERR_INVALID_ARG for unknown bits. */
+#define MF_DEBUG_DROP_FWD_KV 1
+#define MF_DEBUG_DROP_BWD_QDO 2
+MF_API mf_status mf_debug_inject(int32_t flags);
+
 /* Static description of a status code. */
 MF_API const char *mf_status_string(mf_status status);
 

@@ -17,8 +17,8 @@ import os
 import torch
 
 __all__ = ["MfError", "Plan", "pack_plan", "attn_fwd", "attn_bwd", "check", "record_main_kernel", "lib",
-           "library_path",
-           "EXPORTED_SYMBOLS", "STATUS"]
+           "library_path", "fwd_workspace_bytes", "bwd_workspace_bytes", "debug_inject",
+           "DEBUG_DROP_FWD_KV", "DEBUG_DROP_BWD_QDO", "EXPORTED_SYMBOLS", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libmf.so")
@@ -28,7 +28,7 @@ STATUS = {0: "MF_OK", 1: "MF_ERR_INVALID_ARG", 2: "MF_ERR_UNSUPPORTED", 3: "MF_E
 
 EXPORTED_SYMBOLS = ["mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd_workspace_size", "mf_attn_fwd",
                     "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_attn_bwd_noalloc", "mf_check",
-                    "mf_record_main_kernel",
+                    "mf_record_main_kernel", "mf_debug_inject",
                     "mf_status_string", "mf_last_cuda_error"]
 
 TILE = 128
@@ -83,12 +83,14 @@ def lib():
                               ctypes.c_float, c_vp, c_sz, c_vp, c_vp, c_vp, c_vp]
     L.mf_check.argtypes = [ctypes.POINTER(MfPlan), c_vp]
     L.mf_record_main_kernel.argtypes = [c_vp, c_vp]
+    L.mf_debug_inject.argtypes = [c_i32]
     L.mf_status_string.argtypes = [c_i32]
     L.mf_status_string.restype = ctypes.c_char_p
     L.mf_last_cuda_error.argtypes = []
     L.mf_last_cuda_error.restype = ctypes.c_char_p
     for name in ("mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd_workspace_size", "mf_attn_fwd",
-                 "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_record_main_kernel"):
+                 "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_record_main_kernel",
+                 "mf_debug_inject"):
         getattr(L, name).restype = c_i32
     _lib = L
     return L
@@ -251,6 +253,17 @@ def record_main_kernel(start=None, stop=None, stream=None):
     else:
         a = b = None
     _raise(lib().mf_record_main_kernel(a, b), "mf_record_main_kernel")
+
+
+DEBUG_DROP_FWD_KV = 1
+DEBUG_DROP_BWD_QDO = 2
+
+
+def debug_inject(flags: int = 0):
+    """Timeout-path test aid (see mf_debug_inject): while set, the attention
+    calls of this thread drop their streamed-tile loads so that their bounded
+    waits run out and check() raises MF_ERR_TIMEOUT.  0 restores normal use."""
+    _raise(lib().mf_debug_inject(int(flags)), "mf_debug_inject")
 
 
 def check(plan: Plan, stream=None):

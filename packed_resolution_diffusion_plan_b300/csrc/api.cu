@@ -18,6 +18,10 @@ thread_local std::string g_last_cuda_error;
 // One-shot event pair set by mf_record_main_kernel, consumed by the next
 // attention call on this thread.
 thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+// Load-dropping flags of mf_debug_inject (MF_DEBUG_*), passed to the kernels.
+static_assert(MF_DEBUG_DROP_FWD_KV == mf::kDebugDropFwdKV && MF_DEBUG_DROP_BWD_QDO == mf::kDebugDropBwdQdo,
+              "debug flag values");
+thread_local int32_t g_debug_flags = 0;
 
 void take_events(cudaEvent_t* a, cudaEvent_t* b) {
   *a = g_ev_start;
@@ -182,6 +186,7 @@ mf::AttnGeom make_geom(const mf_plan* plan, int32_t heads) {
   g.heads = heads;
   g.n_items = plan->n_tiles * heads;
   g.status = plan->status;
+  g.debug = g_debug_flags;
   return g;
 }
 
@@ -409,5 +414,11 @@ const char* mf_status_string(mf_status status) {
 }
 
 const char* mf_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+mf_status mf_debug_inject(int32_t flags) {
+  if (flags & ~(MF_DEBUG_DROP_FWD_KV | MF_DEBUG_DROP_BWD_QDO)) return MF_ERR_INVALID_ARG;
+  g_debug_flags = flags;
+  return MF_OK;
+}
 
 }  // extern "C"

@@ -311,21 +311,26 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tma_load_2d(smem + C::kOffV + h * 16384, &tv, &c.kv_full, xcol + h * 64, kv0);
       }
       int nq_issued = 0, ndo_issued = 0;
+      const bool drop = (args.g.debug & kDebugDropBwdQdo) != 0;  // timeout-path tests only
       for (int i = 0; i < n_q; ++i) {
         const int s = i & 1;
         const uint32_t ph_free = ((i >> 1) - 1) & 1;  // completion i/2 - 1 of the slot's free barrier
         const int y = w.seq_start + i * kTile;
         if (i >= 2 && !mbar_wait(&c.q_free[s], ph_free, abort_flag)) break;
-        mbar_arrive_expect_tx(&c.q_full[s], C::kTileBytes);
-        for (int h = 0; h < C::kHalves; ++h)
-          tma_load_2d(smem + C::kOffQ + s * C::kTileBytes + h * 16384, &tq, &c.q_full[s], xcol + h * 64, y);
-        nq_issued = i + 1;
+        if (!drop) {
+          mbar_arrive_expect_tx(&c.q_full[s], C::kTileBytes);
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_2d(smem + C::kOffQ + s * C::kTileBytes + h * 16384, &tq, &c.q_full[s], xcol + h * 64, y);
+          nq_issued = i + 1;
+        }
         // dO_i reuses the one slot once dV_{i-1} has read dO_{i-1}.
         if (i >= 1 && !mbar_wait(&c.do_free, (i - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&c.do_full, C::kTileBytes);
-        for (int h = 0; h < C::kHalves; ++h)
-          tma_load_2d(smem + C::kOffDO + h * 16384, &tdo, &c.do_full, xcol + h * 64, y);
-        ndo_issued = i + 1;
+        if (!drop) {
+          mbar_arrive_expect_tx(&c.do_full, C::kTileBytes);
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_2d(smem + C::kOffDO + h * 16384, &tdo, &c.do_full, xcol + h * 64, y);
+          ndo_issued = i + 1;
+        }
         if (i >= 2) mbar_arrive(&c.q_issued);  // the refill of the slot and dO_i are in the TMA queue
       }
       // Let this CTA's own copies land before its shared memory is released.

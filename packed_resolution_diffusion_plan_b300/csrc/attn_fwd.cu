@@ -177,27 +177,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                       q0 + a * kTile);
       int k_issued = 0, v_issued = 0;
       bool ok = true;
+      const bool drop = (args.g.debug & kDebugDropFwdKV) != 0;  // timeout-path tests only
       // K_j goes out one step ahead of V_j: the logit MMAs need it first.
       for (int j = 0; ok && j <= n_kv; ++j) {
         const int jk = j;  // K tile issued in this step
         if (jk < n_kv) {
           const int s = jk % C::kKStages;
           if (jk >= C::kKStages && !mbar_wait(&bar_k_free[s], (jk / C::kKStages - 1) & 1, &s_abort)) break;
-          mbar_arrive_expect_tx(&bar_k_full[s], C::kTileBytes);
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_2d(smem + C::kOffK + s * C::kTileBytes + h * 16384, &tk, &bar_k_full[s], xcol + h * 64,
-                        w.seq_start + jk * kTile);
-          k_issued = jk + 1;
+          if (!drop) {
+            mbar_arrive_expect_tx(&bar_k_full[s], C::kTileBytes);
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_2d(smem + C::kOffK + s * C::kTileBytes + h * 16384, &tk, &bar_k_full[s], xcol + h * 64,
+                          w.seq_start + jk * kTile);
+            k_issued = jk + 1;
+          }
         }
         const int jv = j - 1;  // V tile issued in this step
         if (jv >= 0) {
           const int s = jv % C::kVStages;
           if (jv >= C::kVStages && !mbar_wait(&bar_v_free[s], (jv / C::kVStages - 1) & 1, &s_abort)) break;
-          mbar_arrive_expect_tx(&bar_v_full[s], C::kTileBytes);
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_2d(smem + C::kOffV + s * C::kTileBytes + h * 16384, &tv, &bar_v_full[s], xcol + h * 64,
-                        w.seq_start + jv * kTile);
-          v_issued = jv + 1;
+          if (!drop) {
+            mbar_arrive_expect_tx(&bar_v_full[s], C::kTileBytes);
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_2d(smem + C::kOffV + s * C::kTileBytes + h * 16384, &tv, &bar_v_full[s], xcol + h * 64,
+                          w.seq_start + jv * kTile);
+            v_issued = jv + 1;
+          }
         }
       }
       // Let this CTA's own copies land before its shared memory is released.

@@ -45,6 +45,12 @@ cudaError_t launch_pack_plan(const PlanArgs& a, cudaStream_t stream);
 // length (longest first), the sample index, its first 128-row tile index and
 // its first 256-row tile-pair index in that order; a CTA item is (sorted
 // sample, head, tile or pair) with the tile / pair fastest.
+// AttnGeom::debug bits (the C ABI's MF_DEBUG_* values): the TMA producer of
+// the forward / backward main kernel drops its streamed-tile loads, so that
+// the consumers' bounded waits run out (tests of the timeout path).
+constexpr int32_t kDebugDropFwdKV = 1;
+constexpr int32_t kDebugDropBwdQdo = 2;
+
 struct AttnGeom {
   const int32_t* cu_seqlens;
   const int32_t* pos;
@@ -55,6 +61,7 @@ struct AttnGeom {
   int32_t heads;
   int32_t n_items;          // work units (tiles or pairs) * heads
   int32_t* status;
+  int32_t debug;            // MF_DEBUG_* flags of mf_debug_inject (0 in normal use)
 };
 
 struct FwdArgs {

@@ -113,3 +113,6 @@ def test_attn_validation_without_gpu(L):
     empty.head_dim = 128
     assert L.mf_attn_fwd(None, None, None, ctypes.byref(empty), 2, 128, 0.0, None, 0, None, None, None) == 0
     assert L.mf_check(None, None) == 1
+    # the timeout-path test aid takes only the documented bits
+    assert L.mf_debug_inject(4) == 1 and L.mf_debug_inject(-1) == 1
+    assert L.mf_debug_inject(3) == 0 and L.mf_debug_inject(0) == 0
