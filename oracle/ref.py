@@ -20,6 +20,13 @@ What it computes, and where each step comes from:
   pair (2i, 2i+1) of each half at frequency theta^(-2i/(head_dim/2)),
   theta = 10000, rotation x0' = x0 cos - x1 sin, x1' = x0 sin + x1 cos; text
   tokens are not rotated.
+* ``rope`` with ``rope_axes=3`` -- the edit model's (h, w, f) positions
+  (Mage-Flow review, section on the editing model: a frame dimension is added
+  to the 2D RoPE so that source and target latents are told apart).  The
+  pages give no layout; this library fixes it: head_dim split into three
+  contiguous slices, frame | row | col, of head_dim/8, 7 head_dim/16 and
+  7 head_dim/16 dimensions; pair i of an a-dimension slice turns at
+  theta^(-2i/a) times the token's index on that axis.
 * ``attn_fwd`` / ``attn_bwd`` -- joint text+image self-attention of each
   sample (review, "Native-Resolution MMDiT": text and image tokens are
   concatenated and processed by joint self-attention), i.e. plain
@@ -48,24 +55,30 @@ TEXT_POS = -1
 # --------------------------------------------------------------------------
 
 def pack_plan(samples, token_budget: int = 0):
-    """Plan a pack from per-sample (text_len, height_px, width_px).
+    """Plan a pack from per-sample (text_len, height_px, width_px[, frames]).
 
-    The samples are taken in order; the pack is the longest prefix whose total
-    token count stays within ``token_budget`` (0 = no budget).  Tokens of one
-    sample are [text; image], the image in row-major latent order (row = index
-    along the height).  Returns a dict with ``n_samples`` (packed prefix),
-    ``cu_seqlens`` int32 [n+1], ``pos`` int32 [T, 2] ((-1, -1) for text),
-    ``total_tokens``, ``max_seqlen`` and ``max_grid`` (largest grid side).
-    Raises ValueError for invalid shapes and when not even the first sample
-    fits the budget.
+    ``frames`` (default 1) is 1 for a generation sample and 2 for an edit
+    sample, whose source and target latents (same size) follow its text as
+    frames 0 and 1.  The samples are taken in order; the pack is the longest
+    prefix whose total token count stays within ``token_budget`` (0 = no
+    budget).  Tokens of one sample are [text; frame 0; frame 1 ...], each
+    frame in row-major latent order (row = index along the height).  Returns
+    a dict with ``n_samples`` (packed prefix), ``cu_seqlens`` int32 [n+1],
+    ``pos`` int32 [T, 2] ((-1, -1) for text), ``frame`` int32 [T] (-1 for
+    text), ``total_tokens``, ``max_seqlen`` and ``max_grid`` (largest grid
+    side).  Raises ValueError for invalid shapes and when not even the first
+    sample fits the budget.
     """
-    lens, grids = [], []
-    for (t, h, w) in samples:
-        if t < 0 or h <= 0 or w <= 0 or h % PATCH or w % PATCH:
-            raise ValueError(f"invalid sample {(t, h, w)}")
+    lens, grids, frames = [], [], []
+    for smp in samples:
+        t, h, w = smp[:3]
+        nf = smp[3] if len(smp) > 3 else 1
+        if t < 0 or h <= 0 or w <= 0 or h % PATCH or w % PATCH or nf not in (1, 2):
+            raise ValueError(f"invalid sample {tuple(smp)}")
         gh, gw = h // PATCH, w // PATCH
-        lens.append(t + gh * gw)
+        lens.append(t + nf * gh * gw)
         grids.append((gh, gw))
+        frames.append(nf)
     n = 0
     used = 0
     for L in lens:
@@ -80,16 +93,20 @@ def pack_plan(samples, token_budget: int = 0):
         cu[i + 1] = cu[i] + lens[i]
     T = int(cu[n])
     pos = np.full((T, 2), TEXT_POS, dtype=np.int32)
+    frame = np.full(T, TEXT_POS, dtype=np.int32)
     for i in range(n):
         t = samples[i][0]
         gh, gw = grids[i]
-        for j in range(gh * gw):
-            pos[cu[i] + t + j, 0] = j // gw
-            pos[cu[i] + t + j, 1] = j % gw
+        for j in range(frames[i] * gh * gw):
+            f, r = divmod(j, gh * gw)
+            pos[cu[i] + t + j, 0] = r // gw
+            pos[cu[i] + t + j, 1] = r % gw
+            frame[cu[i] + t + j] = f
     return {
         "n_samples": n,
         "cu_seqlens": cu,
         "pos": pos,
+        "frame": frame,
         "total_tokens": T,
         "max_seqlen": int(max(lens[:n])) if n else 0,
         "max_grid": int(max(max(g) for g in grids[:n])) if n else 0,
@@ -100,35 +117,51 @@ def pack_plan(samples, token_budget: int = 0):
 # 2D RoPE
 # --------------------------------------------------------------------------
 
-def rope_angles(pos, head_dim: int, theta: float = 10000.0):
+def rope_axes_dims(head_dim: int, rope_axes: int):
+    """Sizes of the contiguous head_dim slices and the position axis each
+    turns by: 2 axes -> [(row, d/2), (col, d/2)]; 3 axes -> [(frame, d/8),
+    (row, 7d/16), (col, 7d/16)]."""
+    if rope_axes == 2:
+        return [("row", head_dim // 2), ("col", head_dim // 2)]
+    if rope_axes == 3:
+        a = 7 * head_dim // 16
+        return [("frame", head_dim - 2 * a), ("row", a), ("col", a)]
+    raise ValueError(f"rope_axes must be 2 or 3, got {rope_axes}")
+
+
+def rope_angles(pos, head_dim: int, theta: float = 10000.0, frame=None, rope_axes: int = 2):
     """Angle of every rotation pair: [T, head_dim/2] float64.
 
-    Pair index p < head_dim/4 lives in the first half and turns by
-    row * f_p; pair index head_dim/4 + p lives in the second half and turns by
-    col * f_p, with f_p = theta^(-2p/(head_dim/2)).  Text rows get angle 0.
+    The head is cut into the slices of ``rope_axes_dims``; pair i of a slice
+    of a dimensions turns by (the token's index on that slice's axis) *
+    theta^(-2i/a).  With 2 axes that is: pair p < head_dim/4 in the first
+    half turns by row * f_p, pair head_dim/4 + p by col * f_p, with
+    f_p = theta^(-2p/(head_dim/2)).  Text rows get angle 0.
     """
-    half = head_dim // 2
-    nfreq = half // 2
-    f = np.array([theta ** (-2.0 * p / half) for p in range(nfreq)], dtype=np.float64)
     pos = np.asarray(pos)
-    row = pos[:, 0].astype(np.float64)
-    col = pos[:, 1].astype(np.float64)
-    ang = np.concatenate([row[:, None] * f[None, :], col[:, None] * f[None, :]], axis=1)
+    idx = {"row": pos[:, 0].astype(np.float64), "col": pos[:, 1].astype(np.float64)}
+    if frame is not None:
+        idx["frame"] = np.asarray(frame).astype(np.float64)
+    parts = []
+    for axis, a in rope_axes_dims(head_dim, rope_axes):
+        f = np.array([theta ** (-2.0 * i / a) for i in range(a // 2)], dtype=np.float64)
+        parts.append(idx[axis][:, None] * f[None, :])
+    ang = np.concatenate(parts, axis=1)
     ang[pos[:, 0] < 0] = 0.0
     return ang
 
 
-def rope(x, pos, theta: float = 10000.0, inverse: bool = False):
-    """Rotate x [T, heads, head_dim] by each token's 2D position.
+def rope(x, pos, theta: float = 10000.0, inverse: bool = False, frame=None, rope_axes: int = 2):
+    """Rotate x [T, heads, head_dim] by each token's 2D (or (h, w, f)) position.
 
     Pair m covers dims (2m, 2m+1) over the whole head (m < head_dim/2), which
     puts the first head_dim/4 pairs in the first half and the rest in the
-    second half.  ``inverse`` rotates by the negated angles (R^T), which is
-    the adjoint needed to pull gradients back to un-rotated inputs.
+    second half (2 axes).  ``inverse`` rotates by the negated angles (R^T),
+    which is the adjoint needed to pull gradients back to un-rotated inputs.
     """
     x = np.asarray(x, dtype=np.float64)
     T, H, D = x.shape
-    ang = rope_angles(pos, D, theta)
+    ang = rope_angles(pos, D, theta, frame, rope_axes)
     if inverse:
         ang = -ang
     c = np.cos(ang)[:, None, :]
@@ -154,10 +187,12 @@ def _logsumexp_rows(S):
     return (m + np.log(np.exp(S - m).sum(axis=1, keepdims=True)))[:, 0]
 
 
-def attn_fwd(q, k, v, cu_seqlens, pos, softmax_scale: float = 0.0, theta: float = 10000.0):
+def attn_fwd(q, k, v, cu_seqlens, pos, softmax_scale: float = 0.0, theta: float = 10000.0,
+             frame=None, rope_axes: int = 2):
     """Per-sample, per-head softmax attention on RoPE-rotated q and k.
 
-    q, k, v: [T, H, D] (any float dtype, widened to float64).
+    q, k, v: [T, H, D] (any float dtype, widened to float64).  ``frame`` and
+    ``rope_axes`` select the (h, w, f) rotation (see ``rope``).
     Returns O [T, H, D] float64 and LSE [H, T] float64, where LSE is the
     natural log-sum-exp of the scaled logits of each query row.
     """
@@ -166,8 +201,8 @@ def attn_fwd(q, k, v, cu_seqlens, pos, softmax_scale: float = 0.0, theta: float 
     v = np.asarray(v, dtype=np.float64)
     T, H, D = q.shape
     s = softmax_scale if softmax_scale > 0 else default_scale(D)
-    qr = rope(q, pos, theta)
-    kr = rope(k, pos, theta)
+    qr = rope(q, pos, theta, frame=frame, rope_axes=rope_axes)
+    kr = rope(k, pos, theta, frame=frame, rope_axes=rope_axes)
     O = np.zeros((T, H, D))
     LSE = np.zeros((H, T))
     for i in range(len(cu_seqlens) - 1):
@@ -182,7 +217,7 @@ def attn_fwd(q, k, v, cu_seqlens, pos, softmax_scale: float = 0.0, theta: float 
 
 
 def attn_bwd(q, k, v, o, lse, do, cu_seqlens, pos, softmax_scale: float = 0.0,
-             theta: float = 10000.0):
+             theta: float = 10000.0, frame=None, rope_axes: int = 2):
     """Gradients dQ, dK, dV of sum(O * dO) w.r.t. the un-rotated q, k, v.
 
     With q~ = R q, k~ = R k, S = s q~ k~^T, P = exp(S - LSE):
@@ -199,8 +234,8 @@ def attn_bwd(q, k, v, o, lse, do, cu_seqlens, pos, softmax_scale: float = 0.0,
     do = np.asarray(do, dtype=np.float64)
     T, H, D = q.shape
     s = softmax_scale if softmax_scale > 0 else default_scale(D)
-    qr = rope(q, pos, theta)
-    kr = rope(k, pos, theta)
+    qr = rope(q, pos, theta, frame=frame, rope_axes=rope_axes)
+    kr = rope(k, pos, theta, frame=frame, rope_axes=rope_axes)
     dqr = np.zeros((T, H, D))
     dkr = np.zeros((T, H, D))
     dv = np.zeros((T, H, D))
@@ -215,8 +250,8 @@ def attn_bwd(q, k, v, o, lse, do, cu_seqlens, pos, softmax_scale: float = 0.0,
             dS = P * (dP - Drow[:, None])
             dqr[a:b, h, :] = s * (dS @ kr[a:b, h, :])
             dkr[a:b, h, :] = s * (dS.T @ qr[a:b, h, :])
-    dq = rope(dqr, pos, theta, inverse=True)
-    dk = rope(dkr, pos, theta, inverse=True)
+    dq = rope(dqr, pos, theta, inverse=True, frame=frame, rope_axes=rope_axes)
+    dk = rope(dkr, pos, theta, inverse=True, frame=frame, rope_axes=rope_axes)
     return dq, dk, dv
 
 

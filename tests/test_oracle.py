@@ -172,6 +172,117 @@ def test_rope_single_axis_is_1d_rope():
 
 
 # --------------------------------------------------------------------------
+# (h, w, f) RoPE of edit packs
+# --------------------------------------------------------------------------
+
+def test_pack_plan_edit_frames():
+    """An edit sample (text, H, W, 2) carries its source and target latents as
+    frames 0 and 1 after its text, each in row-major order (hand-derived)."""
+    p = oracle.pack_plan([(5, 32, 48, 2), (2, 16, 16)])   # grids 2x3 (two frames), 1x1
+    assert list(p["cu_seqlens"]) == [0, 17, 20]
+    assert p["total_tokens"] == 20 and p["max_seqlen"] == 17 and p["max_grid"] == 3
+    want_pos = [(-1, -1)] * 5 + [(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 2)] * 2 + [(-1, -1)] * 2 + [(0, 0)]
+    assert [tuple(r) for r in p["pos"]] == want_pos
+    assert list(p["frame"]) == [-1] * 5 + [0] * 6 + [1] * 6 + [-1, -1, 0]
+    with pytest.raises(ValueError):
+        oracle.pack_plan([(1, 16, 16, 3)])
+
+
+def test_rope3d_golden_angles():
+    rows = np.loadtxt(os.path.join(GOLDEN, "rope3d_angles_d32.txt"))
+    for r, c, f, *ang in rows:
+        pos = np.array([[int(r), int(c)]], dtype=np.int32)
+        frame = np.array([int(f)], dtype=np.int32)
+        for m, a in zip((0, 1, 2, 3, 9, 10), ang):
+            x = np.zeros((1, 1, 32))
+            x[0, 0, 2 * m] = 1.0
+            y = oracle.rope(x, pos, frame=frame, rope_axes=3)[0, 0]
+            got = math.atan2(y[2 * m + 1], y[2 * m])
+            assert abs(got - math.remainder(a, 2 * math.pi)) < 1e-12, (r, c, f, m)
+            assert np.all(np.delete(y, [2 * m, 2 * m + 1]) == 0)
+
+
+def test_rope3d_axes_dims():
+    assert oracle.rope_axes_dims(128, 3) == [("frame", 16), ("row", 56), ("col", 56)]
+    assert oracle.rope_axes_dims(64, 3) == [("frame", 8), ("row", 28), ("col", 28)]
+    assert oracle.rope_axes_dims(128, 2) == [("row", 64), ("col", 64)]
+
+
+def test_rope3d_norm_inverse_and_text():
+    rng = np.random.default_rng(4)
+    pos = np.array([[-1, -1], [0, 0], [5, 9], [127, 3], [40, 127]], dtype=np.int32)
+    frame = np.array([-1, 1, 0, 1, 1], dtype=np.int32)
+    x = rng.standard_normal((5, 3, 128))
+    y = oracle.rope(x, pos, frame=frame, rope_axes=3)
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), atol=1e-12)
+    assert np.allclose(oracle.rope(y, pos, inverse=True, frame=frame, rope_axes=3), x, atol=1e-12)
+    assert np.array_equal(y[0], x[0])
+
+
+def test_rope3d_relative_position_including_frame():
+    rng = np.random.default_rng(5)
+    D = 128
+    q = rng.standard_normal((1, 1, D))
+    k = rng.standard_normal((1, 1, D))
+    p, pp = np.array([[3, 11]]), np.array([[7, 2]])
+    f, ff = np.array([1]), np.array([0])
+    base = (oracle.rope(q, p, frame=f, rope_axes=3) * oracle.rope(k, pp, frame=ff, rope_axes=3)).sum()
+    for dr, dc, df in [(1, 0, 0), (0, 5, 0), (0, 0, 1), (13, 21, 3)]:
+        d = np.array([[dr, dc]])
+        moved = (oracle.rope(q, p + d, frame=f + df, rope_axes=3) *
+                 oracle.rope(k, pp + d, frame=ff + df, rope_axes=3)).sum()
+        assert abs(moved - base) < 1e-10
+    # the frame does tell source from target: same (row, col), other frame
+    other = (oracle.rope(q, p, frame=f, rope_axes=3) * oracle.rope(k, p, frame=ff, rope_axes=3)).sum()
+    same = (oracle.rope(q, p, frame=ff, rope_axes=3) * oracle.rope(k, p, frame=ff, rope_axes=3)).sum()
+    assert abs(other - same) > 1e-6
+
+
+def test_rope3d_frame_slice_is_1d_rope():
+    """Row = col = 0 everywhere: the row and column slices are untouched and
+    the frame slice (head_dim/8 dims) is the textbook 1D RoPE of its pairs,
+    written here in complex form."""
+    rng = np.random.default_rng(6)
+    D, theta = 128, 10000.0
+    a = D // 8
+    x = rng.standard_normal((4, 2, D))
+    pos = np.zeros((4, 2), dtype=np.int32)
+    frame = np.array([0, 1, 2, 5], dtype=np.int32)
+    y = oracle.rope(x, pos, frame=frame, rope_axes=3)
+    assert np.array_equal(y[..., a:], x[..., a:])
+    f = theta ** (-np.arange(a // 2) * 2.0 / a)
+    z = x[..., 0:a:2] + 1j * x[..., 1:a:2]
+    zr = z * np.exp(1j * frame[:, None, None] * f[None, None, :])
+    assert np.allclose(y[..., 0:a:2], zr.real, atol=1e-12)
+    assert np.allclose(y[..., 1:a:2], zr.imag, atol=1e-12)
+
+
+def test_bwd3d_central_finite_differences():
+    """The exact gradient with the (h, w, f) rotation: directional central
+    differences on a small edit pack (two frames) plus a one-frame sample."""
+    samples = [(3, 32, 32, 2), (2, 16, 48)]
+    p = oracle.pack_plan(samples)
+    rng = np.random.default_rng(7)
+    T = p["total_tokens"]
+    q, k, v, g = (rng.standard_normal((T, 2, 64)) for _ in range(4))
+    kw = dict(frame=p["frame"], rope_axes=3)
+    O, L = oracle.attn_fwd(q, k, v, p["cu_seqlens"], p["pos"], **kw)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, O, L, g, p["cu_seqlens"], p["pos"], **kw)
+
+    def loss(q_, k_, v_):
+        return float((oracle.attn_fwd(q_, k_, v_, p["cu_seqlens"], p["pos"], **kw)[0] * g).sum())
+
+    eps = 1e-6
+    for x, dx in ((q, dq), (k, dk), (v, dv)):
+        u = rng.standard_normal(x.shape)
+        ap = [x + eps * u if y is x else y for y in (q, k, v)]
+        am = [x - eps * u if y is x else y for y in (q, k, v)]
+        fd = (loss(*ap) - loss(*am)) / (2 * eps)
+        an = float((dx * u).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (fd, an)
+
+
+# --------------------------------------------------------------------------
 # forward
 # --------------------------------------------------------------------------
 
