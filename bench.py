@@ -54,8 +54,14 @@ def parse_args():
     return ap.parse_args()
 
 
+def sample_len(smp):
+    """Tokens of one (text_len, height_px, width_px[, frames]) sample."""
+    frames = smp[3] if len(smp) > 3 else 1
+    return smp[0] + frames * (smp[1] // 16) * (smp[2] // 16)
+
+
 def pack_flops(samples, heads, head_dim):
-    lens = [t + (h // 16) * (w // 16) for (t, h, w) in samples]
+    lens = [sample_len(s) for s in samples]
     s2 = float(sum(L * L for L in lens))
     fwd = 4.0 * heads * head_dim * s2
     return fwd, 2.5 * fwd, lens
@@ -148,7 +154,7 @@ def oracle_sample(wl, seconds, max_heads=None):
     """Time the oracle's fwd+bwd on one sample of the workload, head after
     head, until `seconds` of CPU work (or all heads) are done."""
     import oracle
-    lens = [t + (h // 16) * (w // 16) for (t, h, w) in wl.samples]
+    lens = [sample_len(s) for s in wl.samples]
     # the sample whose length is closest to 3,600 tokens: large enough to be
     # representative, small enough that one head takes about a second
     si = int(np.argmin([abs(L - 3600) for L in lens]))
@@ -162,8 +168,9 @@ def oracle_sample(wl, seconds, max_heads=None):
     t0 = time.perf_counter()
     while True:
         q, k, v, do = (torch.randn(shape, generator=g).to(torch.bfloat16).double().numpy() for _ in range(4))
-        O, L = oracle.attn_fwd(q, k, v, p["cu_seqlens"], p["pos"])
-        oracle.attn_bwd(q, k, v, O, L, do, p["cu_seqlens"], p["pos"])
+        rope = dict(frame=p["frame"], rope_axes=wl.rope_axes)
+        O, L = oracle.attn_fwd(q, k, v, p["cu_seqlens"], p["pos"], **rope)
+        oracle.attn_bwd(q, k, v, O, L, do, p["cu_seqlens"], p["pos"], **rope)
         heads += 1
         flop += 3.5 * 4.0 * wl.head_dim * n * n
         el = time.perf_counter() - t0
@@ -264,7 +271,8 @@ def run_mf(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
-        plan = mf.pack_plan(wl.samples, token_budget=wl.token_budget, head_dim=D, device=dev)
+        plan = mf.pack_plan(wl.samples, token_budget=wl.token_budget, head_dim=D, device=dev,
+                            rope_axes=wl.rope_axes)
         if ev is not None:
             mf.record_main_kernel(ev[0], ev[1])
         mf.attn_fwd(q, k, v, plan, out=o, lse=lse, workspace=ws_fwd)

@@ -75,11 +75,15 @@ typedef enum {
 } mf_status;
 
 /* One sample of a pack: text length in tokens, image height and width in
- * pixels (positive multiples of 16). */
+ * pixels (positive multiples of 16), and its latent frames: 1 (or 0) for a
+ * generation sample, 2 for an edit sample, whose source and target latents
+ * (the same size) follow its text as frames 0 and 1 (review, editing-model
+ * section: (h, w, f) positions tell source tokens from target tokens). */
 typedef struct {
   int32_t text_len;
   int32_t height;
   int32_t width;
+  int32_t frames;
 } mf_sample;
 
 /* Largest supported pack (samples) and latent grid side. */
@@ -100,7 +104,13 @@ typedef struct {
   int32_t n_pairs;      /* sum_i ceil(L_i / (2 * MF_TILE)): forward work units */
   int32_t *cu_seqlens;  /* device int32 [n_samples + 1], exclusive scan of L_i */
   int32_t *pos;         /* device int32 [total_tokens][2]: (row, col); text = (-1, -1) */
-  float *rope_cs;       /* device float32 [max_grid][head_dim/4][2]: cos, sin of p*f_i */
+  int32_t *frame;       /* device int32 [total_tokens]: latent frame; text = -1 */
+  int32_t rope_axes;    /* 2: (row, col) RoPE; 3: (frame, row, col) RoPE */
+  float *rope_cs;       /* device float32 [grid][a/2][2]: cos, sin of p * theta^(-2i/a) for the
+                           row/col slices of a dims (a = head_dim/2 with 2 axes, 7 head_dim/16
+                           with 3), grid > max_grid */
+  float *rope_f;        /* device float32 [2][head_dim/16][2]: the frame slice's table (3 axes;
+                           NULL with 2) */
   int32_t *order;       /* device int32 [n_samples][4]: (sample, first tile, first tile pair, 0),
                            longest sample first */
   int32_t *status;      /* device int32 status word written by kernels that time out */
@@ -109,7 +119,8 @@ typedef struct {
 /* Bytes of device workspace mf_pack_plan needs for this request.  Validates
  * the request like mf_pack_plan (same error codes); `samples` is host memory. */
 MF_API mf_status mf_pack_plan_workspace_size(const mf_sample *samples, int32_t n_samples,
-                                      int32_t token_budget, int32_t head_dim, size_t *bytes);
+                                      int32_t token_budget, int32_t head_dim, int32_t rope_axes,
+                                      size_t *bytes);
 
 /* Plan a pack (review, section "Native-Resolution MMDiT": variable-length
  * latent token rows packed under a fixed token budget, unpadded text, per-
@@ -117,6 +128,12 @@ MF_API mf_status mf_pack_plan_workspace_size(const mf_sample *samples, int32_t n
  * token count is <= token_budget is packed (token_budget 0 = no budget).
  *   samples      host array [n_samples]; 0 <= n_samples <= MF_MAX_SAMPLES
  *   head_dim     64 or 128 (sizes the RoPE table)
+ *   rope_axes    2: the first half of head_dim turns by the latent row, the
+ *                second by the column; 3: head_dim is cut into frame | row |
+ *                col slices of head_dim/8, 7 head_dim/16 and 7 head_dim/16
+ *                dims (the edit model's (h, w, f) positions).  Pair i of an
+ *                a-dim slice turns at theta^(-2i/a) times the token's index on
+ *                that axis.  Edit samples (frames = 2) need 3.
  *   rope_theta   RoPE base (> 0; 10000 is the usual value)
  *   workspace    device memory of at least mf_pack_plan_workspace_size bytes,
  *                256-byte aligned
@@ -124,10 +141,11 @@ MF_API mf_status mf_pack_plan_workspace_size(const mf_sample *samples, int32_t n
  * Runs a device prefix scan, the per-token id expansion and the RoPE table on
  * `stream`, then synchronizes `stream` once to read the scalars back.
  * Errors: MF_ERR_INVALID_ARG (null pointer, text_len < 0, H or W not a
- * positive multiple of 16, total tokens >= 2^31, short or misaligned
- * workspace), MF_ERR_UNSUPPORTED, MF_ERR_BUDGET, MF_ERR_CUDA. */
+ * positive multiple of 16, frames not in {0, 1, 2}, frames = 2 with
+ * rope_axes 2, rope_axes not 2 or 3, total tokens >= 2^31, short or
+ * misaligned workspace), MF_ERR_UNSUPPORTED, MF_ERR_BUDGET, MF_ERR_CUDA. */
 MF_API mf_status mf_pack_plan(const mf_sample *samples, int32_t n_samples, int32_t token_budget,
-                       int32_t head_dim, float rope_theta, void *workspace,
+                       int32_t head_dim, int32_t rope_axes, float rope_theta, void *workspace,
                        size_t workspace_bytes, mf_plan *plan_out, void *stream);
 
 /* Bytes of device workspace mf_attn_fwd needs: fp16 rotated copies

@@ -256,7 +256,7 @@ def attn_bwd(q, k, v, o, lse, do, cu_seqlens, pos, softmax_scale: float = 0.0,
 
 
 def attn_rows(q, k, v, cu_seqlens, pos, rows, head: int, softmax_scale: float = 0.0,
-              theta: float = 10000.0):
+              theta: float = 10000.0, frame=None, rope_axes: int = 2):
     """O and LSE of selected query rows of one head, one row at a time.
 
     For full-size packs: each row touches only its own sample's keys, so it
@@ -273,8 +273,10 @@ def attn_rows(q, k, v, cu_seqlens, pos, rows, head: int, softmax_scale: float = 
     for n, r in enumerate(rows):
         i = int(np.searchsorted(cu, r, side="right") - 1)
         a, b = int(cu[i]), int(cu[i + 1])
-        qr = rope(q[r:r + 1], pos[r:r + 1], theta)[0, 0]
-        kr = rope(k[a:b], pos[a:b], theta)[:, 0, :]
+        fq = None if frame is None else frame[r:r + 1]
+        fk = None if frame is None else frame[a:b]
+        qr = rope(q[r:r + 1], pos[r:r + 1], theta, frame=fq, rope_axes=rope_axes)[0, 0]
+        kr = rope(k[a:b], pos[a:b], theta, frame=fk, rope_axes=rope_axes)[:, 0, :]
         srow = s * (kr @ qr)
         m = srow.max()
         lse = m + math.log(np.exp(srow - m).sum())

@@ -35,7 +35,8 @@ TILE = 128
 
 
 class MfSample(ctypes.Structure):
-    _fields_ = [("text_len", ctypes.c_int32), ("height", ctypes.c_int32), ("width", ctypes.c_int32)]
+    _fields_ = [("text_len", ctypes.c_int32), ("height", ctypes.c_int32), ("width", ctypes.c_int32),
+                ("frames", ctypes.c_int32)]
 
 
 class MfPlan(ctypes.Structure):
@@ -43,9 +44,9 @@ class MfPlan(ctypes.Structure):
                 ("max_seqlen", ctypes.c_int32), ("max_grid", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
                 ("n_pairs", ctypes.c_int32),
-                ("cu_seqlens", ctypes.c_void_p), ("pos", ctypes.c_void_p),
-                ("rope_cs", ctypes.c_void_p), ("order", ctypes.c_void_p),
-                ("status", ctypes.c_void_p)]
+                ("cu_seqlens", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("frame", ctypes.c_void_p),
+                ("rope_axes", ctypes.c_int32), ("rope_cs", ctypes.c_void_p), ("rope_f", ctypes.c_void_p),
+                ("order", ctypes.c_void_p), ("status", ctypes.c_void_p)]
 
 
 class MfError(RuntimeError):
@@ -71,9 +72,9 @@ def lib():
                            "`python -m packed_resolution_diffusion_plan_b300.build`")
     L = ctypes.CDLL(library_path)
     c_i32, c_vp, c_sz = ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
-    L.mf_pack_plan_workspace_size.argtypes = [ctypes.POINTER(MfSample), c_i32, c_i32, c_i32,
+    L.mf_pack_plan_workspace_size.argtypes = [ctypes.POINTER(MfSample), c_i32, c_i32, c_i32, c_i32,
                                               ctypes.POINTER(c_sz)]
-    L.mf_pack_plan.argtypes = [ctypes.POINTER(MfSample), c_i32, c_i32, c_i32, ctypes.c_float, c_vp,
+    L.mf_pack_plan.argtypes = [ctypes.POINTER(MfSample), c_i32, c_i32, c_i32, c_i32, ctypes.c_float, c_vp,
                                c_sz, ctypes.POINTER(MfPlan), c_vp]
     L.mf_attn_fwd_workspace_size.argtypes = [c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]
     L.mf_attn_fwd.argtypes = [c_vp, c_vp, c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32, ctypes.c_float,
@@ -110,8 +111,9 @@ def _stream_ptr(stream, device):
 
 def _samples_array(samples):
     arr = (MfSample * max(1, len(samples)))()
-    for i, (t, h, w) in enumerate(samples):
-        arr[i] = MfSample(int(t), int(h), int(w))
+    for i, smp in enumerate(samples):
+        t, h, w = smp[:3]
+        arr[i] = MfSample(int(t), int(h), int(w), int(smp[3]) if len(smp) > 3 else 1)
     return arr
 
 
@@ -129,6 +131,7 @@ class Plan:
     max_seqlen = property(lambda self: self.raw.max_seqlen)
     max_grid = property(lambda self: self.raw.max_grid)
     head_dim = property(lambda self: self.raw.head_dim)
+    rope_axes = property(lambda self: self.raw.rope_axes)
     n_tiles = property(lambda self: self.raw.n_tiles)
     n_pairs = property(lambda self: self.raw.n_pairs)
 
@@ -147,26 +150,39 @@ class Plan:
     def pos(self) -> torch.Tensor:
         return self._view(self.raw.pos, 2 * self.total_tokens, torch.int32).view(-1, 2)
 
+    def frame(self) -> torch.Tensor:
+        """Latent frame of each token (-1 for text)."""
+        return self._view(self.raw.frame, self.total_tokens, torch.int32)
+
+    def rope_table_frame(self) -> torch.Tensor:
+        """The frame slice's table of a 3-axis plan: [2, head_dim/16, 2] (cos, sin)."""
+        assert self.rope_axes == 3
+        n = 2 * (self.head_dim // 16) * 2
+        return self._view(self.raw.rope_f, n, torch.float32).view(2, self.head_dim // 16, 2)
+
     def rope_table(self) -> torch.Tensor:
-        n = self.max_grid * (self.head_dim // 4) * 2
-        return self._view(self.raw.rope_cs, n, torch.float32).view(self.max_grid, self.head_dim // 4, 2)
+        """The row/col table: [max_grid, a/2, 2] (cos, sin), a = the row/col slice width."""
+        nh = self.head_dim // 4 if self.rope_axes == 2 else 7 * self.head_dim // 32
+        n = self.max_grid * nh * 2
+        return self._view(self.raw.rope_cs, n, torch.float32).view(self.max_grid, nh, 2)
 
     def order(self) -> torch.Tensor:
         return self._view(self.raw.order, 4 * self.n_samples, torch.int32).view(-1, 4)
 
 
 def pack_plan(samples, token_budget: int = 0, head_dim: int = 128, rope_theta: float = 10000.0,
-              device=None, stream=None) -> Plan:
-    """Plan a pack of (text_len, height_px, width_px) samples on the GPU."""
+              device=None, stream=None, rope_axes: int = 2) -> Plan:
+    """Plan a pack of (text_len, height_px, width_px[, frames]) samples on the
+    GPU; rope_axes 3 selects the (frame, row, col) rotation of edit packs."""
     L = lib()
     device = torch.device(device if device is not None else "cuda")
     arr = _samples_array(samples)
     nbytes = ctypes.c_size_t(0)
-    _raise(L.mf_pack_plan_workspace_size(arr, len(samples), int(token_budget), int(head_dim),
+    _raise(L.mf_pack_plan_workspace_size(arr, len(samples), int(token_budget), int(head_dim), int(rope_axes),
                                          ctypes.byref(nbytes)), "mf_pack_plan_workspace_size")
     ws = torch.empty(max(256, nbytes.value), dtype=torch.uint8, device=device)
     raw = MfPlan()
-    _raise(L.mf_pack_plan(arr, len(samples), int(token_budget), int(head_dim), float(rope_theta),
+    _raise(L.mf_pack_plan(arr, len(samples), int(token_budget), int(head_dim), int(rope_axes), float(rope_theta),
                           ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.byref(raw),
                           _stream_ptr(stream, device)), "mf_pack_plan")
     return Plan(raw, ws, samples, token_budget)

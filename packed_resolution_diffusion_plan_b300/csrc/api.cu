@@ -42,13 +42,17 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // ---------------------------------------------------------------- plan
 struct PlanLayout {
-  size_t off_scalars, off_samples, off_cu, off_order, off_pos, off_rope, bytes;
+  size_t off_scalars, off_samples, off_cu, off_order, off_pos, off_frame, off_rope, off_rope_f, bytes;
   int32_t token_bound, grid_bound;
 };
 
+// Latent frames of a sample (0 counts as 1).
+int32_t sample_frames(const mf_sample& s) { return s.frames == 0 ? 1 : s.frames; }
+
 mf_status check_samples(const mf_sample* samples, int32_t n, int32_t budget, int32_t head_dim,
-                        PlanLayout* L) {
+                        int32_t rope_axes, PlanLayout* L) {
   if (n < 0 || (n > 0 && samples == nullptr) || budget < 0) return MF_ERR_INVALID_ARG;
+  if (rope_axes != 2 && rope_axes != 3) return MF_ERR_INVALID_ARG;
   if (n > MF_MAX_SAMPLES) return MF_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
   long long used = 0;
@@ -58,10 +62,11 @@ mf_status check_samples(const mf_sample* samples, int32_t n, int32_t budget, int
     const mf_sample& s = samples[i];
     if (s.text_len < 0 || s.height <= 0 || s.width <= 0 || (s.height % 16) || (s.width % 16))
       return MF_ERR_INVALID_ARG;
+    if (s.frames < 0 || s.frames > 2 || (sample_frames(s) == 2 && rope_axes != 3)) return MF_ERR_INVALID_ARG;
     const long long gh = s.height / 16, gw = s.width / 16;
     if (gh > MF_MAX_GRID || gw > MF_MAX_GRID) return MF_ERR_UNSUPPORTED;
     gmax = static_cast<int32_t>(std::max<long long>(gmax, std::max(gh, gw)));
-    const long long len = s.text_len + gh * gw;
+    const long long len = s.text_len + sample_frames(s) * gh * gw;
     if (!stopped) {
       if (budget > 0 && used + len > budget) {
         stopped = true;
@@ -78,15 +83,21 @@ mf_status check_samples(const mf_sample* samples, int32_t n, int32_t budget, int
   L->off_scalars = off;
   off = align_up(off + sizeof(PlanScalars), 256);
   L->off_samples = off;
-  off = align_up(off + static_cast<size_t>(n) * 3 * sizeof(int32_t), 256);
+  off = align_up(off + static_cast<size_t>(n) * sizeof(mf_sample), 256);
   L->off_cu = off;
   off = align_up(off + static_cast<size_t>(n + 1) * sizeof(int32_t), 256);
   L->off_order = off;
   off = align_up(off + static_cast<size_t>(n) * 4 * sizeof(int32_t), 256);
   L->off_pos = off;
   off = align_up(off + static_cast<size_t>(L->token_bound) * 2 * sizeof(int32_t), 256);
+  L->off_frame = off;
+  off = align_up(off + static_cast<size_t>(L->token_bound) * sizeof(int32_t), 256);
   L->off_rope = off;
-  off = align_up(off + static_cast<size_t>(gmax) * (head_dim / 4) * 2 * sizeof(float), 256);
+  // row/col table: pairs of the a-dim slices (a = head_dim/2 with 2 axes, 7 head_dim/16 with 3)
+  const int a = rope_axes == 3 ? 7 * head_dim / 16 : head_dim / 2;
+  off = align_up(off + static_cast<size_t>(gmax) * (a / 2) * 2 * sizeof(float), 256);
+  L->off_rope_f = off;
+  if (rope_axes == 3) off = align_up(off + static_cast<size_t>(2) * (head_dim / 16) * 2 * sizeof(float), 256);
   L->bytes = off;
   return MF_OK;
 }
@@ -166,9 +177,10 @@ mf_status check_attn_common(const mf_plan* plan, int32_t heads, int32_t head_dim
   if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
   if (head_dim != plan->head_dim) return MF_ERR_INVALID_ARG;
   if (plan->total_tokens < 0 || plan->n_samples < 0) return MF_ERR_INVALID_ARG;
+  if (plan->rope_axes != 2 && plan->rope_axes != 3) return MF_ERR_INVALID_ARG;
   if (plan->total_tokens > 0 &&
-      (plan->cu_seqlens == nullptr || plan->pos == nullptr || plan->rope_cs == nullptr ||
-       plan->order == nullptr || plan->status == nullptr))
+      (plan->cu_seqlens == nullptr || plan->pos == nullptr || plan->frame == nullptr || plan->rope_cs == nullptr ||
+       (plan->rope_axes == 3 && plan->rope_f == nullptr) || plan->order == nullptr || plan->status == nullptr))
     return MF_ERR_INVALID_ARG;
   if (static_cast<long long>(plan->n_tiles) * heads >= (1ll << 31)) return MF_ERR_UNSUPPORTED;
   if (plan->n_pairs < 0 || plan->n_pairs > plan->n_tiles) return MF_ERR_INVALID_ARG;
@@ -180,6 +192,9 @@ mf::AttnGeom make_geom(const mf_plan* plan, int32_t heads) {
   g.cu_seqlens = plan->cu_seqlens;
   g.pos = plan->pos;
   g.rope_cs = plan->rope_cs;
+  g.rope_f = plan->rope_f;
+  g.frame = plan->frame;
+  g.rope_axes = plan->rope_axes;
   g.order = plan->order;
   g.n_samples = plan->n_samples;
   g.total_tokens = plan->total_tokens;
@@ -201,23 +216,23 @@ constexpr float kLog2e = 1.4426950408889634f;
 extern "C" {
 
 mf_status mf_pack_plan_workspace_size(const mf_sample* samples, int32_t n_samples, int32_t token_budget,
-                                      int32_t head_dim, size_t* bytes) {
+                                      int32_t head_dim, int32_t rope_axes, size_t* bytes) {
   if (bytes == nullptr) return MF_ERR_INVALID_ARG;
   PlanLayout L;
-  mf_status st = check_samples(samples, n_samples, token_budget, head_dim, &L);
+  mf_status st = check_samples(samples, n_samples, token_budget, head_dim, rope_axes, &L);
   if (st != MF_OK) return st;
   *bytes = L.bytes;
   return MF_OK;
 }
 
 mf_status mf_pack_plan(const mf_sample* samples, int32_t n_samples, int32_t token_budget, int32_t head_dim,
-                       float rope_theta, void* workspace, size_t workspace_bytes, mf_plan* plan_out,
-                       void* stream) {
+                       int32_t rope_axes, float rope_theta, void* workspace, size_t workspace_bytes,
+                       mf_plan* plan_out, void* stream) {
   if (plan_out == nullptr || workspace == nullptr) return MF_ERR_INVALID_ARG;
   if (!(rope_theta > 0.f) || !std::isfinite(rope_theta)) return MF_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MF_ERR_INVALID_ARG;
   PlanLayout L;
-  mf_status st = check_samples(samples, n_samples, token_budget, head_dim, &L);
+  mf_status st = check_samples(samples, n_samples, token_budget, head_dim, rope_axes, &L);
   if (st != MF_OK) return st;
   if (workspace_bytes < L.bytes) return MF_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -230,10 +245,13 @@ mf_status mf_pack_plan(const mf_sample* samples, int32_t n_samples, int32_t toke
   a.cu_seqlens = reinterpret_cast<int32_t*>(ws + L.off_cu);
   a.order = reinterpret_cast<int32_t*>(ws + L.off_order);
   a.pos = reinterpret_cast<int32_t*>(ws + L.off_pos);
+  a.frame = reinterpret_cast<int32_t*>(ws + L.off_frame);
   a.token_bound = L.token_bound;
   a.rope_cs = reinterpret_cast<float*>(ws + L.off_rope);
+  a.rope_f = reinterpret_cast<float*>(ws + L.off_rope_f);
   a.grid_bound = L.grid_bound;
   a.head_dim = head_dim;
+  a.rope_axes = rope_axes;
   a.theta = rope_theta;
   cudaError_t e;
   if (n_samples > 0) {
@@ -257,7 +275,10 @@ mf_status mf_pack_plan(const mf_sample* samples, int32_t n_samples, int32_t toke
   plan_out->n_pairs = sc.n_pairs;
   plan_out->cu_seqlens = a.cu_seqlens;
   plan_out->pos = a.pos;
+  plan_out->frame = a.frame;
+  plan_out->rope_axes = rope_axes;
   plan_out->rope_cs = a.rope_cs;
+  plan_out->rope_f = rope_axes == 3 ? a.rope_f : nullptr;
   plan_out->order = a.order;
   plan_out->status = &a.scalars->status;
   return MF_OK;

@@ -105,7 +105,6 @@ struct BwdCfg {
 template <int D>
 __global__ void bwd_pre_kernel(const BwdArgs a) {
   constexpr int kChunks = D / 8;
-  constexpr int nf = D / 4;
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long rows = static_cast<long long>(a.g.total_tokens) * a.g.heads;
   const long long row = gid / kChunks;
@@ -127,24 +126,15 @@ __global__ void bwd_pre_kernel(const BwdArgs a) {
     float4* z = reinterpret_cast<float4*>(a.dq_acc) + gid * 2;
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    // (cos, sin) of the chunk's four pairs: the first D/2 columns turn by the
-    // latent row, the rest by the column; text tokens are not rotated.
+    // the chunk's four rotation pairs (rope_pair_cs; text is not rotated)
     const int2 p = reinterpret_cast<const int2*>(a.g.pos)[tok];
-    float cs[8] = {1.f, 0.f, 1.f, 0.f, 1.f, 0.f, 1.f, 0.f};
-    if (p.x >= 0) {
-      const int dim0 = ch * 8;
-      const int k0 = (dim0 % (D / 2)) / 2;
-      const int pp = dim0 >= D / 2 ? p.y : p.x;
-      const float4* tab = reinterpret_cast<const float4*>(a.g.rope_cs) + static_cast<size_t>(pp) * (nf / 2) + k0 / 2;
-      const float4 c0 = __ldg(tab), c1 = __ldg(tab + 1);
-      cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
-      cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
-    }
+    const int fr = a.g.frame[tok];
     uint32_t qo[4], ko[4];
     float amax = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float c = cs[2 * e], sn = cs[2 * e + 1];
+      const float2 cs = rope_pair_cs<D>(a.g, 4 * ch + e, p, fr);
+      const float c = cs.x, sn = cs.y;
       const float q0 = bf16_lo(qw[e]), q1 = bf16_hi(qw[e]);
       const float k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
       const float yq0 = fmaf(q0, c, -q1 * sn), yq1 = fmaf(q0, sn, q1 * c);
@@ -173,7 +163,6 @@ __global__ void bwd_pre_kernel(const BwdArgs a) {
 template <int D>
 __global__ void bwd_dq_kernel(const BwdArgs a) {
   constexpr int kChunks = D / 8;
-  constexpr int nf = D / 4;
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long rows = static_cast<long long>(a.g.total_tokens) * a.g.heads;
   if (gid >= rows * kChunks) return;
@@ -184,17 +173,13 @@ __global__ void bwd_dq_kernel(const BwdArgs a) {
   const float4 x0 = src[0], x1 = src[1];
   float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
   const int2 p = reinterpret_cast<const int2*>(a.g.pos)[tok];
+  const int fr = a.g.frame[tok];
   uint32_t out[4];
   if (p.x >= 0) {
-    const int dim0 = ch * 8;
-    const int k0 = (dim0 % (D / 2)) / 2;
-    const int pp = dim0 >= D / 2 ? p.y : p.x;
-    const float4* tab = reinterpret_cast<const float4*>(a.g.rope_cs) + static_cast<size_t>(pp) * (nf / 2) + k0 / 2;
-    const float4 c0 = __ldg(tab), c1 = __ldg(tab + 1);
-    const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float c = cs[2 * e], s = cs[2 * e + 1];
+      const float2 cs = rope_pair_cs<D>(a.g, 4 * ch + e, p, fr);
+      const float c = cs.x, s = cs.y;
       const float u0 = x[2 * e] * kLn2, u1 = x[2 * e + 1] * kLn2;
       out[e] = pack_bf16(fmaf(u0, c, u1 * s), fmaf(-u0, s, u1 * c));
     }
@@ -206,27 +191,20 @@ __global__ void bwd_dq_kernel(const BwdArgs a) {
 }
 
 // ---------------------------------------------------------------- bwd_main
-// 32 fp32 TMEM values of a row chunk -> R^T(p) (mult * v) as bf16 stored at dst.
-// The chunk covers columns col0..col0+31 of a D-column row.
+// 32 fp32 TMEM values of a row chunk -> R^T(p, f) (mult * v) as bf16 stored at
+// dst (or mult * v without the rotation).  The chunk covers columns
+// col0..col0+31 of a D-column row, i.e. rotation pairs col0/2 .. col0/2 + 15.
 template <int D>
 __device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32_t (&v)[32], int col0, float mult,
-                                                int2 p, const float* rope_cs, bool inverse_rope) {
-  constexpr int nf = D / 4;
+                                                int2 p, int f, const AttnGeom& g, bool inverse_rope) {
   uint32_t packed[16];
   if (inverse_rope && p.x >= 0) {
-    const int k0 = (col0 % (D / 2)) / 2;  // 16 pairs starting at frequency k0
-    const int pp = col0 >= D / 2 ? p.y : p.x;
-    const float4* tab = reinterpret_cast<const float4*>(rope_cs) + static_cast<size_t>(pp) * (nf / 2) + k0 / 2;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 cs = __ldg(tab + q);  // pairs 2q, 2q+1
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float c = e ? cs.z : cs.x, s = e ? cs.w : cs.y;
-        const int m = 2 * q + e;
-        const float u0 = __uint_as_float(v[2 * m]) * mult, u1 = __uint_as_float(v[2 * m + 1]) * mult;
-        packed[m] = pack_bf16(fmaf(u0, c, u1 * s), fmaf(-u0, s, u1 * c));
-      }
+    for (int m = 0; m < 16; ++m) {
+      const float2 cs = rope_pair_cs<D>(g, col0 / 2 + m, p, f);
+      const float c = cs.x, s = cs.y;
+      const float u0 = __uint_as_float(v[2 * m]) * mult, u1 = __uint_as_float(v[2 * m + 1]) * mult;
+      packed[m] = pack_bf16(fmaf(u0, c, u1 * s), fmaf(-u0, s, u1 * c));
     }
   } else {
 #pragma unroll
@@ -632,6 +610,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       tc_fence_after();
       const size_t rowoff = (static_cast<size_t>(kv0 + r) * args.g.heads + w.head) * D;
       const int2 pk = kv_valid ? reinterpret_cast<const int2*>(args.g.pos)[kv0 + r] : make_int2(-1, -1);
+      const int fk = kv_valid ? args.g.frame[kv0 + r] : -1;
 #pragma unroll 1
       for (int cc = 0; cc < D / 64; ++cc) {
         const int col0 = cw * (D / 2) + 32 * cc;
@@ -639,7 +618,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tmem_ld32(tl + C::kColDV + col0, v);
         tmem_wait_ld(v);
         if (kv_valid)
-          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dv) + rowoff, v, col0, 1.0f, pk, args.g.rope_cs,
+          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dv) + rowoff, v, col0, 1.0f, pk, fk, args.g,
                              false);
       }
 #pragma unroll 1
@@ -650,8 +629,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tmem_wait_ld(v);
         // TMEM holds dS^T q~; dk~ = s dS^T q~.
         if (kv_valid)
-          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dk) + rowoff, v, col0, args.scale, pk,
-                             args.g.rope_cs, true);
+          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dk) + rowoff, v, col0, args.scale, pk, fk,
+                             args.g, true);
       }
     }
   }

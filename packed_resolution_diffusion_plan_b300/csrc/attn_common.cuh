@@ -57,6 +57,28 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// (cos, sin) of rotation pair m (dims 2m, 2m+1, m < D/2) of a token at latent
+// position p = (row, col) and frame f; text tokens (p.x < 0) are not rotated.
+//   2 axes: pairs [0, D/4) turn by the row, [D/4, D/2) by the column; pair i
+//           of a half at theta^(-2i/(D/2)) (plan table [grid][D/4]).
+//   3 axes: pairs [0, D/16) turn by the frame (a slice of D/8 dims, table
+//           [2][D/16]), the next 7D/32 by the row and the last 7D/32 by the
+//           column (slices of 7D/16 dims, table [grid][7D/32]); pair i of an
+//           a-dim slice at theta^(-2i/a).
+template <int D>
+__device__ __forceinline__ float2 rope_pair_cs(const AttnGeom& g, int m, int2 p, int f) {
+  if (p.x < 0) return make_float2(1.f, 0.f);
+  const float2* hw = reinterpret_cast<const float2*>(g.rope_cs);
+  if (g.rope_axes == 3) {
+    constexpr int nf = D / 16, nh = 7 * D / 32;
+    if (m < nf) return __ldg(reinterpret_cast<const float2*>(g.rope_f) + f * nf + m);
+    m -= nf;
+    return m < nh ? __ldg(hw + p.x * nh + m) : __ldg(hw + p.y * nh + (m - nh));
+  }
+  constexpr int nh = D / 4;
+  return m < nh ? __ldg(hw + p.x * nh + m) : __ldg(hw + p.y * nh + (m - nh));
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }

@@ -69,12 +69,11 @@ static_assert(2 * kRegsSoftmax + kRegsCtrl <= 3 * 168, "warpgroup register share
 
 // ---------------------------------------------------------------- fwd_pre
 // One thread per (token, head, 8-column chunk): the chunk's four rotation
-// pairs of q and k (the first D/2 columns turn by the latent row, the rest by
-// the column; text tokens are not rotated), rounded to fp16.
+// pairs of q and k (rope_pair_cs: by the latent row and column, and with 3
+// axes the frame; text tokens are not rotated), rounded to fp16.
 template <int D>
 __global__ void fwd_pre_kernel(const FwdArgs a) {
   constexpr int kChunks = D / 8;
-  constexpr int nf = D / 4;
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long rows = static_cast<long long>(a.g.total_tokens) * a.g.heads;
   if (gid >= rows * kChunks) return;
@@ -85,21 +84,13 @@ __global__ void fwd_pre_kernel(const FwdArgs a) {
   const uint32_t* qw = reinterpret_cast<const uint32_t*>(&qv);
   const uint32_t* kw = reinterpret_cast<const uint32_t*>(&kv);
   const int2 p = reinterpret_cast<const int2*>(a.g.pos)[tok];
-  float cs[8] = {1.f, 0.f, 1.f, 0.f, 1.f, 0.f, 1.f, 0.f};
-  if (p.x >= 0) {
-    const int dim0 = ch * 8;
-    const int k0 = (dim0 % (D / 2)) / 2;
-    const int pp = dim0 >= D / 2 ? p.y : p.x;
-    const float4* tab = reinterpret_cast<const float4*>(a.g.rope_cs) + static_cast<size_t>(pp) * (nf / 2) + k0 / 2;
-    const float4 c0 = __ldg(tab), c1 = __ldg(tab + 1);
-    cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
-    cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
-  }
+  const int fr = a.g.frame[tok];
   uint32_t qo[4], ko[4];
   float amax = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float c = cs[2 * e], sn = cs[2 * e + 1];
+    const float2 cs = rope_pair_cs<D>(a.g, 4 * ch + e, p, fr);
+    const float c = cs.x, sn = cs.y;
     const float q0 = bf16_lo(qw[e]), q1 = bf16_hi(qw[e]);
     const float k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
     const float yq0 = fmaf(q0, c, -q1 * sn) * a.scale_log2, yq1 = fmaf(q0, sn, q1 * c) * a.scale_log2;

@@ -25,17 +25,20 @@ struct PlanScalars {
 };
 
 struct PlanArgs {
-  const int32_t* samples;   // device [n][3] (text_len, height_px, width_px)
+  const int32_t* samples;   // device [n][4] (text_len, height_px, width_px, frames)
   int32_t n;
   int32_t budget;           // 0 = none
   PlanScalars* scalars;
   int32_t* cu_seqlens;      // [n+1]
   int32_t* order;           // [n][4]
   int32_t* pos;             // [token_bound][2]
+  int32_t* frame;           // [token_bound]
   int32_t token_bound;
-  float* rope_cs;           // [grid_bound][head_dim/4][2]
+  float* rope_cs;           // [grid_bound][a/2][2], a = the row/col slice width
+  float* rope_f;            // [2][head_dim/16][2] (3 axes), else unused
   int32_t grid_bound;
   int32_t head_dim;
+  int32_t rope_axes;        // 2 or 3
   float theta;
 };
 
@@ -55,6 +58,9 @@ struct AttnGeom {
   const int32_t* cu_seqlens;
   const int32_t* pos;
   const float* rope_cs;
+  const float* rope_f;
+  const int32_t* frame;
+  int32_t rope_axes;
   const int32_t* order;
   int32_t n_samples;
   int32_t total_tokens;

@@ -58,8 +58,9 @@ __global__ void __launch_bounds__(kPlanThreads) pack_scan_kernel(PlanArgs a) {
     const int i = t * kPerThread + u;
     long long L = 0;
     if (i < a.n) {
-      const int32_t* s = a.samples + 3 * i;
-      L = static_cast<long long>(s[0]) + static_cast<long long>(s[1] / 16) * (s[2] / 16);
+      const int32_t* s = a.samples + 4 * i;
+      const int frames = s[3] == 0 ? 1 : s[3];
+      L = static_cast<long long>(s[0]) + static_cast<long long>(frames) * (s[1] / 16) * (s[2] / 16);
       s_len[i] = static_cast<int32_t>(L);
     }
     mine[u] = L;
@@ -77,7 +78,7 @@ __global__ void __launch_bounds__(kPlanThreads) pack_scan_kernel(PlanArgs a) {
         a.cu_seqlens[i] = static_cast<int32_t>(off);
         atomicAdd(&s_npacked, 1);
         atomicMax(&s_maxlen, static_cast<int>(mine[u]));
-        const int32_t* s = a.samples + 3 * i;
+        const int32_t* s = a.samples + 4 * i;
         atomicMax(&s_maxgrid, max(s[1] / 16, s[2] / 16));
       }
       off += mine[u];
@@ -141,7 +142,9 @@ __global__ void __launch_bounds__(kPlanThreads) pack_scan_kernel(PlanArgs a) {
   }
 }
 
-// Per-token ids: text -> (-1, -1); image token j -> (j / gw, j % gw).
+// Per-token ids: text -> (-1, -1), frame -1; image token j of a sample with
+// gh x gw latents per frame -> frame j / (gh gw), then (r / gw, r % gw) with
+// r = j % (gh gw).
 __global__ void pack_pos_kernel(PlanArgs a) {
   const int tok = blockIdx.x * blockDim.x + threadIdx.x;
   const int total = a.scalars->total_tokens;
@@ -152,28 +155,48 @@ __global__ void pack_pos_kernel(PlanArgs a) {
     const int mid = (lo + hi) >> 1;
     if (a.cu_seqlens[mid] <= tok) lo = mid; else hi = mid;
   }
-  const int32_t* s = a.samples + 3 * lo;
+  const int32_t* s = a.samples + 4 * lo;
   const int j = tok - a.cu_seqlens[lo] - s[0];
   int2 p = make_int2(-1, -1);
+  int f = -1;
   if (j >= 0) {
-    const int gw = s[2] / 16;
-    p = make_int2(j / gw, j % gw);
+    const int gw = s[2] / 16, per_frame = (s[1] / 16) * gw;
+    f = j / per_frame;
+    const int r = j - f * per_frame;
+    p = make_int2(r / gw, r % gw);
   }
   reinterpret_cast<int2*>(a.pos)[tok] = p;
+  a.frame[tok] = f;
 }
 
-// cos/sin(p * f_i), f_i = theta^(-2i/(head_dim/2)), i < head_dim/4, for
-// p < grid_bound ([p][i] order).  Angles and sin/cos are evaluated in double
-// and rounded to float once.
+// cos/sin(p * theta^(-2i/a)) for the row/col slices of a dims (a = head_dim/2
+// with 2 axes, 7 head_dim/16 with 3), i < a/2, p < grid_bound ([p][i] order);
+// with 3 axes also the frame slice's (a_f = head_dim/8 dims) for frames 0, 1
+// ([f][i] order, after the row/col entries in the index space).  Angles and
+// sin/cos are evaluated in double and rounded to float once.
 __global__ void rope_table_kernel(PlanArgs a) {
-  const int nf = a.head_dim / 4;
+  const int a_hw = a.rope_axes == 3 ? 7 * a.head_dim / 16 : a.head_dim / 2;
+  const int a_f = a.head_dim / 8;
+  const int n_hw = a.grid_bound * (a_hw / 2);
+  const int n_f = a.rope_axes == 3 ? 2 * (a_f / 2) : 0;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= a.grid_bound * nf) return;
-  const int p = idx / nf, i = idx % nf;
-  const double f = pow(static_cast<double>(a.theta), -2.0 * i / (a.head_dim / 2));
+  if (idx >= n_hw + n_f) return;
+  int p, i, width;
+  if (idx < n_hw) {
+    p = idx / (a_hw / 2);
+    i = idx % (a_hw / 2);
+    width = a_hw;
+  } else {
+    p = (idx - n_hw) / (a_f / 2);
+    i = (idx - n_hw) % (a_f / 2);
+    width = a_f;
+  }
+  const double f = pow(static_cast<double>(a.theta), -2.0 * i / width);
   double sv, cv;
   sincos(static_cast<double>(p) * f, &sv, &cv);
-  reinterpret_cast<float2*>(a.rope_cs)[idx] = make_float2(static_cast<float>(cv), static_cast<float>(sv));
+  const float2 v = make_float2(static_cast<float>(cv), static_cast<float>(sv));
+  if (idx < n_hw) reinterpret_cast<float2*>(a.rope_cs)[idx] = v;
+  else reinterpret_cast<float2*>(a.rope_f)[idx - n_hw] = v;
 }
 
 }  // namespace
@@ -187,7 +210,8 @@ cudaError_t launch_pack_plan(const PlanArgs& a, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int nt = a.grid_bound * (a.head_dim / 4);
+  const int a_hw = a.rope_axes == 3 ? 7 * a.head_dim / 16 : a.head_dim / 2;
+  const int nt = a.grid_bound * (a_hw / 2) + (a.rope_axes == 3 ? a.head_dim / 8 : 0);
   if (a.grid_bound > 0) {
     rope_table_kernel<<<(nt + 255) / 256, 256, 0, stream>>>(a);
     e = cudaGetLastError();

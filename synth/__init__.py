@@ -43,10 +43,13 @@ class Workload:
     notes: str = ""
     seed: int = 0
     extra: dict = field(default_factory=dict)
+    rope_axes: int = 2       # 3: the (frame, row, col) rotation of edit packs
 
     def segments(self):
-        """Per-sample (text rows, image rows) counts in pack order."""
-        return [(t, (h // PATCH) * (w // PATCH)) for (t, h, w) in self.samples]
+        """Per-sample (text rows, image rows) counts in pack order (an edit
+        sample (t, h, w, 2) has two frames of image rows)."""
+        return [(smp[0], (smp[3] if len(smp) > 3 else 1) * (smp[1] // PATCH) * (smp[2] // PATCH))
+                for smp in self.samples]
 
     @property
     def total_tokens(self) -> int:
@@ -121,12 +124,28 @@ def extreme_aspect(seed: int = 0) -> Workload:
                     notes="parts sum to 25,096 tokens (the stated 24,840 omits the 2048^2 text)")
 
 
+def edit_pack(seed: int = 0) -> Workload:
+    """An edit training pack (not one of the five headline configs): three
+    edit samples whose source and target latents (frames 0 and 1, same size)
+    follow their instruction text, plus one generation sample, drawn like the
+    training pack (sides 512-1536 px, text 32-256 tokens) until about 24K
+    tokens; (frame, row, col) RoPE."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(4):
+        gh, gw = (int(x) for x in rng.integers(32, 97, size=2))
+        t = int(rng.integers(32, 257))
+        out.append((t, gh * PATCH, gw * PATCH, 2 if i < 3 else 1))
+    return Workload("edit_pack", out, heads=24, head_dim=128, passes="fwd+bwd", seed=seed, rope_axes=3)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "single_1024": single_1024,
     "native_res_32k": native_res,
     "cfg_pair": cfg_pair,
     "extreme_aspect": extreme_aspect,
+    "edit_pack": edit_pack,
 }
 
 
@@ -156,10 +175,12 @@ def draw_tensors(wl: Workload, with_grad: bool = True):
     return out
 
 
-def random_pack(seed: int, n_samples: int, max_text: int, max_side_tokens: int):
+def random_pack(seed: int, n_samples: int, max_text: int, max_side_tokens: int, edit: bool = False):
     """Small random packs for edge-case parity tests: ragged lengths, image-only
     samples (text 0) and single-token samples (text 0, 16x16 px).  Every sample
-    has at least one image token.  Returns [(text_len, height_px, width_px)].
+    has at least one image token.  Returns [(text_len, height_px, width_px)],
+    or with ``edit`` [(text_len, height_px, width_px, frames)] with frames
+    drawn from {1, 2}.
     """
     rng = np.random.default_rng(seed)
     out = []
@@ -167,5 +188,8 @@ def random_pack(seed: int, n_samples: int, max_text: int, max_side_tokens: int):
         gh = int(rng.integers(1, max_side_tokens + 1))
         gw = int(rng.integers(1, max_side_tokens + 1))
         t = int(rng.integers(0, max_text + 1))
-        out.append((t, gh * PATCH, gw * PATCH))
+        if edit:
+            out.append((t, gh * PATCH, gw * PATCH, int(rng.integers(1, 3))))
+        else:
+            out.append((t, gh * PATCH, gw * PATCH))
     return out

@@ -38,10 +38,10 @@ def test_status_strings(L):
     assert L.mf_last_cuda_error() is not None
 
 
-def _ws_size(L, samples, budget=0, head_dim=128):
+def _ws_size(L, samples, budget=0, head_dim=128, rope_axes=2):
     arr = mf._samples_array(samples)
     n = ctypes.c_size_t(0)
-    st = L.mf_pack_plan_workspace_size(arr, len(samples), budget, head_dim, ctypes.byref(n))
+    st = L.mf_pack_plan_workspace_size(arr, len(samples), budget, head_dim, rope_axes, ctypes.byref(n))
     return st, n.value
 
 
@@ -56,31 +56,41 @@ def test_plan_validation_without_gpu(L):
     st, n_small = _ws_size(L, [(10, 64, 64)] * 3, budget=60)
     st2, n_all = _ws_size(L, [(10, 64, 64)] * 3)
     assert st == 0 and st2 == 0 and n_small < n_all
+    # frames: an edit sample (frames 2) needs the 3-axis rotation; frames > 2 and
+    # rope_axes other than 2 or 3 are rejected; 0 frames count as one
+    assert _ws_size(L, [(4, 32, 32, 2)], rope_axes=3)[0] == 0
+    assert _ws_size(L, [(4, 32, 32, 2)], rope_axes=2)[0] == 1
+    assert _ws_size(L, [(4, 32, 32, 3)], rope_axes=3)[0] == 1
+    assert _ws_size(L, [(4, 32, 32, 0)])[0] == 0
+    assert _ws_size(L, [(4, 32, 32)], rope_axes=4)[0] == 1
+    assert _ws_size(L, [(4, 512, 512, 2)], rope_axes=3)[1] > _ws_size(L, [(4, 512, 512)], rope_axes=3)[1]
     # null size pointer / null samples with n > 0
-    assert L.mf_pack_plan_workspace_size(None, 1, 0, 128, None) == 1
+    assert L.mf_pack_plan_workspace_size(None, 1, 0, 128, 2, None) == 1
     n = ctypes.c_size_t(0)
-    assert L.mf_pack_plan_workspace_size(None, 2, 0, 128, ctypes.byref(n)) == 1
-    assert L.mf_pack_plan_workspace_size(None, 5000, 0, 128, ctypes.byref(n)) == 1
+    assert L.mf_pack_plan_workspace_size(None, 2, 0, 128, 2, ctypes.byref(n)) == 1
+    assert L.mf_pack_plan_workspace_size(None, 5000, 0, 128, 2, ctypes.byref(n)) == 1
     arr = mf._samples_array([(0, 16, 16)] * 1)
     big = (mf.MfSample * 4097)()
     for i in range(4097):
-        big[i] = mf.MfSample(1, 16, 16)
-    assert L.mf_pack_plan_workspace_size(big, 4097, 0, 128, ctypes.byref(n)) == 2
+        big[i] = mf.MfSample(1, 16, 16, 1)
+    assert L.mf_pack_plan_workspace_size(big, 4097, 0, 128, 2, ctypes.byref(n)) == 2
     # pack call: null / misaligned workspace and bad theta fail before any CUDA call
     plan = mf.MfPlan()
-    assert L.mf_pack_plan(arr, 1, 0, 128, 10000.0, None, 0, ctypes.byref(plan), None) == 1
-    assert L.mf_pack_plan(arr, 1, 0, 128, 10000.0, ctypes.c_void_p(256 + 8), 1 << 20,
+    assert L.mf_pack_plan(arr, 1, 0, 128, 2, 10000.0, None, 0, ctypes.byref(plan), None) == 1
+    assert L.mf_pack_plan(arr, 1, 0, 128, 2, 10000.0, ctypes.c_void_p(256 + 8), 1 << 20,
                           ctypes.byref(plan), None) == 1
-    assert L.mf_pack_plan(arr, 1, 0, 128, -1.0, ctypes.c_void_p(256), 1 << 20,
+    assert L.mf_pack_plan(arr, 1, 0, 128, 2, -1.0, ctypes.c_void_p(256), 1 << 20,
                           ctypes.byref(plan), None) == 1
-    assert L.mf_pack_plan(arr, 1, 0, 128, 10000.0, ctypes.c_void_p(256), 16,
+    assert L.mf_pack_plan(arr, 1, 0, 128, 2, 10000.0, ctypes.c_void_p(256), 16,
+                          ctypes.byref(plan), None) == 1
+    assert L.mf_pack_plan(arr, 1, 0, 128, 5, 10000.0, ctypes.c_void_p(256), 1 << 20,
                           ctypes.byref(plan), None) == 1
 
 
 def test_attn_validation_without_gpu(L):
     plan = mf.MfPlan()
-    plan.total_tokens, plan.n_samples, plan.head_dim, plan.n_tiles = 10, 1, 128, 1
-    for p in ("cu_seqlens", "pos", "rope_cs", "order", "status"):
+    plan.total_tokens, plan.n_samples, plan.head_dim, plan.n_tiles, plan.rope_axes = 10, 1, 128, 1, 2
+    for p in ("cu_seqlens", "pos", "frame", "rope_cs", "order", "status"):
         setattr(plan, p, 4096)
     vp = ctypes.c_void_p
     ok = vp(1 << 20)
@@ -110,7 +120,7 @@ def test_attn_validation_without_gpu(L):
     assert L.mf_attn_bwd_workspace_size(10, 2, 80, ctypes.byref(n)) == 2
     # an empty pack is a no-op that needs no tensors
     empty = mf.MfPlan()
-    empty.head_dim = 128
+    empty.head_dim, empty.rope_axes = 128, 2
     assert L.mf_attn_fwd(None, None, None, ctypes.byref(empty), 2, 128, 0.0, None, 0, None, None, None) == 0
     assert L.mf_check(None, None) == 1
     # the timeout-path test aid takes only the documented bits

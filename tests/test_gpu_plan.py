@@ -13,9 +13,10 @@ import synth
 pytestmark = pytest.mark.gpu
 
 
-def _check_plan(samples, budget, head_dim=128, theta=10000.0):
+def _check_plan(samples, budget, head_dim=128, theta=10000.0, rope_axes=2):
     ref = oracle.pack_plan(samples, budget)
-    p = mf.pack_plan(samples, token_budget=budget, head_dim=head_dim, rope_theta=theta)
+    p = mf.pack_plan(samples, token_budget=budget, head_dim=head_dim, rope_theta=theta, rope_axes=rope_axes)
+    assert p.rope_axes == rope_axes
     mf.check(p)
     assert p.n_samples == ref["n_samples"]
     assert p.total_tokens == ref["total_tokens"]
@@ -23,6 +24,7 @@ def _check_plan(samples, budget, head_dim=128, theta=10000.0):
     assert p.max_grid == ref["max_grid"]
     assert np.array_equal(p.cu_seqlens().cpu().numpy(), ref["cu_seqlens"])
     assert np.array_equal(p.pos().cpu().numpy(), ref["pos"])
+    assert np.array_equal(p.frame().cpu().numpy(), ref["frame"])
     lens = np.diff(ref["cu_seqlens"])
     # work order: longest first, ties by sample index, tile starts = prefix of ceil(L/128)
     order = p.order().cpu().numpy()
@@ -35,21 +37,45 @@ def _check_plan(samples, budget, head_dim=128, theta=10000.0):
         assert list(order[:, 2]) == list(np.concatenate([[0], np.cumsum(pairs)[:-1]]).astype(int))
         assert list(order[:, 3]) == [0] * len(want)
     assert p.n_tiles == sum(tiles) and p.n_pairs == sum(pairs)
-    # RoPE table: cos/sin of p * theta^(-2i/(D/2)) rounded once to float32
+    # RoPE tables: cos/sin of p * theta^(-2i/a) rounded once to float32, a =
+    # the row/col slice width (head_dim/2, or 7 head_dim/16 with 3 axes), and
+    # with 3 axes the frame slice's (a = head_dim/8) for frames 0 and 1
     if p.max_grid:
         tab = p.rope_table().cpu().numpy().astype(np.float64)
-        half = head_dim // 2
-        f = theta ** (-2.0 * np.arange(head_dim // 4) / half)
+        a = head_dim // 2 if rope_axes == 2 else 7 * head_dim // 16
+        f = theta ** (-2.0 * np.arange(a // 2) / a)
         ang = np.arange(p.max_grid)[:, None] * f[None, :]
         assert np.abs(tab[..., 0] - np.cos(ang)).max() < 1e-7
         assert np.abs(tab[..., 1] - np.sin(ang)).max() < 1e-7
+        if rope_axes == 3:
+            tf = p.rope_table_frame().cpu().numpy().astype(np.float64)
+            af = head_dim // 8
+            ff = theta ** (-2.0 * np.arange(af // 2) / af)
+            angf = np.arange(2)[:, None] * ff[None, :]
+            assert np.abs(tf[..., 0] - np.cos(angf)).max() < 1e-7
+            assert np.abs(tf[..., 1] - np.sin(angf)).max() < 1e-7
     return p
 
 
 @pytest.mark.parametrize("name", list(synth.WORKLOADS))
 def test_plan_workloads_bit_exact(name):
     wl = synth.WORKLOADS[name]()
-    _check_plan(wl.samples, wl.token_budget, wl.head_dim)
+    _check_plan(wl.samples, wl.token_budget, wl.head_dim, rope_axes=wl.rope_axes)
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_plan_edit_packs(seed, head_dim):
+    """Random edit packs (frames 1 or 2 per sample) with the (frame, row, col)
+    rotation, and a generation-only pack planned with 3 axes."""
+    _check_plan(synth.random_pack(100 + seed, 9, 40, 12, edit=True), 0, head_dim, rope_axes=3)
+    _check_plan(synth.random_pack(200 + seed, 5, 40, 12), 0, head_dim, rope_axes=3)
+
+
+def test_plan_edit_needs_three_axes():
+    with pytest.raises(mf.MfError) as ei:
+        mf.pack_plan([(4, 32, 32, 2)], rope_axes=2)
+    assert ei.value.code == "MF_ERR_INVALID_ARG"
 
 
 @pytest.mark.parametrize("seed", range(8))
