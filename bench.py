@@ -369,7 +369,7 @@ def run_mf(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "precision": "bf16 inputs/outputs; tcgen05 MMAs with fp32 accumulation (logit products on fp16 "
                      "copies of the rotated Q/K rows, P*V and dO products in bf16)",
-        "config": {"workload": f"{wl.name} seed {wl.seed}", "samples": [list(s) for s in wl.samples],
+        "config": {"workload": f"{wl.name} seed {wl.seed}", "samples": [list(x) for x in wl.samples],
                    "seq_lens": lens, "total_tokens": T, "heads": H, "head_dim": D,
                    "token_budget": wl.token_budget, "fwd_tflop": fwd_flop / 1e12, "bwd_tflop": bwd_flop / 1e12,
                    "step": "pack plan + forward + backward",
@@ -383,6 +383,14 @@ def run_mf(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if wl.name.endswith("_padded"):
+        # the packed pack's own work, done inside the padded batch's time
+        base = synth.WORKLOADS[wl.name[:-len("_padded")]](args.seed)
+        uf, ub, ulens = pack_flops(base.samples, base.heads, base.head_dim)
+        line["padding"] = {"packed_workload": base.name, "packed_tokens": int(sum(ulens)),
+                           "padded_tokens": T, "useful_tflops": job_tflops(world, uf + ub, ms_step),
+                           "note": "value counts the padded batch's work; useful_tflops counts only "
+                                   "the packed samples' work over the same time"}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

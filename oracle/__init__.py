@@ -1,6 +1,6 @@
 """Float64 CPU oracle (test infrastructure only; see ``oracle.ref``)."""
-from .ref import (attn_bwd, attn_fwd, attn_rows, brute_force_masked, default_scale,
+from .ref import (attn_bwd, attn_fwd, attn_rows, brute_force_masked, cfg_combine, default_scale,
                   pack_plan, rope, rope_angles, rope_axes_dims)
 
-__all__ = ["pack_plan", "rope", "rope_angles", "rope_axes_dims", "attn_fwd", "attn_bwd", "attn_rows",
+__all__ = ["pack_plan", "rope", "rope_angles", "rope_axes_dims", "attn_fwd", "attn_bwd", "attn_rows", "cfg_combine",
            "brute_force_masked", "default_scale"]

@@ -33,6 +33,11 @@ What it computes, and where each step comes from:
   softmax(s * q~ k~^T) v per sample and head, with s = 1/sqrt(head_dim) unless
   given; the backward is the exact gradient of that definition with respect
   to the un-rotated q, k and v.
+* ``cfg_combine`` -- classifier-free guidance over a pack whose samples come
+  in (conditional, unconditional) pairs (review, section on CFG: the two
+  branches run in one packed forward).  The pages do not print the
+  combination; the standard reading is taken: guided = u + g (c - u) for the
+  image rows of each pair, written over the conditional sample's image rows.
 * ``brute_force_masked`` -- the thing the offsets replace: dense attention
   over the whole pack with an explicit block-diagonal mask.  Written
   separately from ``attn_fwd`` on purpose.
@@ -283,6 +288,34 @@ def attn_rows(q, k, v, cu_seqlens, pos, rows, head: int, softmax_scale: float = 
         O[n] = np.exp(srow - lse) @ v[a:b]
         LSE[n] = lse
     return O, LSE
+
+
+def cfg_combine(o, cu_seqlens, pos, guidance: float):
+    """Guided outputs of a pack of (cond, uncond) sample pairs.
+
+    ``o`` [T, H, D].  Samples 2p and 2p+1 are the conditional and the
+    unconditional branch of prompt p; their image rows (the rows with
+    pos >= 0, which end each sample) must have the same count.  Returns a
+    float64 copy of ``o`` whose conditional image rows hold
+    u + guidance * (c - u); every other row is unchanged.
+    """
+    o = np.asarray(o, dtype=np.float64)
+    out = o.copy()
+    cu = np.asarray(cu_seqlens)
+    pos = np.asarray(pos)
+    n = len(cu) - 1
+    if n % 2:
+        raise ValueError("a CFG pack holds (cond, uncond) pairs")
+    for p in range(n // 2):
+        ca, cb = int(cu[2 * p]), int(cu[2 * p + 1])
+        ua, ub = int(cu[2 * p + 1]), int(cu[2 * p + 2])
+        c_img = [r for r in range(ca, cb) if pos[r, 0] >= 0]
+        u_img = [r for r in range(ua, ub) if pos[r, 0] >= 0]
+        if len(c_img) != len(u_img):
+            raise ValueError(f"pair {p}: image row counts differ")
+        for rc, ru in zip(c_img, u_img):
+            out[rc] = o[ru] + guidance * (o[rc] - o[ru])
+    return out
 
 
 def brute_force_masked(q, k, v, cu_seqlens, pos, softmax_scale: float = 0.0,

@@ -124,6 +124,29 @@ def extreme_aspect(seed: int = 0) -> Workload:
                     notes="parts sum to 25,096 tokens (the stated 24,840 omits the 2048^2 text)")
 
 
+def native_res_50k(seed: int = 0) -> Workload:
+    """The training-pack recipe at the pages' 50,000 packed tokens per GPU
+    (review, kernel-fusion section: 8 GPUs, global batch 8, ~50K tokens per
+    GPU)."""
+    return Workload("native_res_50k", native_res_shapes(seed, 50000), heads=24,
+                    head_dim=128, passes="fwd+bwd", token_budget=50000, seed=seed)
+
+
+def padded(wl: Workload) -> Workload:
+    """The same samples as a padded batch: every sample grown to the longest
+    one's token count with extra text rows (a dense kernel over a padded
+    batch computes the masked positions too, so this is the padded batch's
+    work; the padding rows are not masked).  No token budget."""
+    segs = wl.segments()
+    L = max(a + b for a, b in segs)
+    out = []
+    for smp, (a, b) in zip(wl.samples, segs):
+        out.append((smp[0] + (L - a - b),) + tuple(smp[1:]))
+    return Workload(wl.name + "_padded", out, wl.heads, wl.head_dim, wl.passes, token_budget=0,
+                    seed=wl.seed, rope_axes=wl.rope_axes,
+                    notes=f"{len(out)} samples padded to {L} tokens")
+
+
 def edit_pack(seed: int = 0) -> Workload:
     """An edit training pack (not one of the five headline configs): three
     edit samples whose source and target latents (frames 0 and 1, same size)
@@ -146,6 +169,9 @@ WORKLOADS = {
     "cfg_pair": cfg_pair,
     "extreme_aspect": extreme_aspect,
     "edit_pack": edit_pack,
+    "native_res_50k": native_res_50k,
+    "native_res_32k_padded": lambda seed=0: padded(native_res(seed)),
+    "native_res_50k_padded": lambda seed=0: padded(native_res_50k(seed)),
 }
 
 

@@ -283,6 +283,37 @@ def test_bwd3d_central_finite_differences():
 
 
 # --------------------------------------------------------------------------
+# classifier-free guidance over (cond, uncond) pairs
+# --------------------------------------------------------------------------
+
+def test_cfg_combine_closed_forms():
+    """guidance 1 keeps the conditional rows, 0 gives the unconditional ones,
+    2 gives the extrapolation 2c - u; text rows and the unconditional sample
+    are untouched; rows pair up from the end of each sample (text lengths
+    differ, image rows match)."""
+    samples = [(5, 32, 48), (2, 32, 48), (3, 16, 16), (0, 16, 16)]
+    p = oracle.pack_plan(samples)
+    rng = np.random.default_rng(8)
+    o = rng.standard_normal((p["total_tokens"], 2, 8))
+    cu = p["cu_seqlens"]
+    c_img = slice(int(cu[0]) + 5, int(cu[1]))
+    u_img = slice(int(cu[1]) + 2, int(cu[2]))
+    for g, want in ((1.0, o[c_img]), (0.0, o[u_img]), (2.0, 2 * o[c_img] - o[u_img])):
+        out = oracle.cfg_combine(o, cu, p["pos"], g)
+        assert np.allclose(out[c_img], want, atol=1e-15)
+        assert np.array_equal(out[int(cu[0]):int(cu[0]) + 5], o[int(cu[0]):int(cu[0]) + 5])
+        assert np.array_equal(out[int(cu[1]):int(cu[2])], o[int(cu[1]):int(cu[2])])
+    # second pair: one image row each, no text in the unconditional sample
+    out = oracle.cfg_combine(o, cu, p["pos"], 3.0)
+    assert np.allclose(out[int(cu[2]) + 3], o[int(cu[3])] + 3.0 * (o[int(cu[2]) + 3] - o[int(cu[3])]))
+    with pytest.raises(ValueError):
+        oracle.cfg_combine(o[:int(cu[3])], cu[:4], p["pos"], 1.0)        # odd sample count
+    q = oracle.pack_plan([(1, 16, 16), (1, 32, 16)])
+    with pytest.raises(ValueError):
+        oracle.cfg_combine(np.zeros((q["total_tokens"], 1, 8)), q["cu_seqlens"], q["pos"], 1.0)
+
+
+# --------------------------------------------------------------------------
 # forward
 # --------------------------------------------------------------------------
 
