@@ -45,6 +45,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mf", "reference"], default="mf")
+    ap.add_argument("--mode", choices=["step", "cfg"], default="step",
+                    help="step: the fwd+bwd training step (the headline); cfg: the CFG pair pack's "
+                         "packed forward + guidance against two separate forwards")
+    ap.add_argument("--guidance", type=float, default=4.0)
     ap.add_argument("--workload", default="native_res_32k", choices=list(synth.WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -433,10 +437,92 @@ def load_traffic(kernel):
         return None
 
 
+def run_cfg(args):
+    """Inference with classifier-free guidance on the CFG pair pack (4 prompts at
+    1024^2, conditional and unconditional branches): one packed forward of both
+    branches followed by the guidance, against two separate forwards (the
+    conditional samples, then the unconditional ones).  The guidance kernel does
+    the same work either way and is timed once, on the packed output."""
+    import packed_resolution_diffusion_plan_b300 as mf
+    dev = torch.device("cuda", 0)
+    wl = synth.cfg_pair(args.seed)
+    host = synth.draw_tensors(wl, with_grad=False)
+    q, k, v = (host[n].to(dev) for n in ("q", "k", "v"))
+    T, H, D = q.shape
+    segs = wl.segments()
+    starts = np.concatenate([[0], np.cumsum([a + b for a, b in segs])]).astype(int)
+    cond_idx = [i for i in range(len(segs)) if i % 2 == 0]
+    unc_idx = [i for i in range(len(segs)) if i % 2 == 1]
+
+    def gather(idx):
+        rows = np.concatenate([np.arange(starts[i], starts[i + 1]) for i in idx])
+        r = torch.as_tensor(rows, device=dev)
+        return [x.index_select(0, r).contiguous() for x in (q, k, v)]
+
+    qc, kc, vc = gather(cond_idx)
+    qu, ku, vu = gather(unc_idx)
+    plan = mf.pack_plan(wl.samples, head_dim=D)
+    plan_c = mf.pack_plan([wl.samples[i] for i in cond_idx], head_dim=D)
+    plan_u = mf.pack_plan([wl.samples[i] for i in unc_idx], head_dim=D)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    oc, lc = torch.empty_like(qc), torch.empty((H, qc.shape[0]), dtype=torch.float32, device=dev)
+    ou, lu = torch.empty_like(qu), torch.empty((H, qu.shape[0]), dtype=torch.float32, device=dev)
+    ws = torch.empty(mf.fwd_workspace_bytes(T, H, D), dtype=torch.uint8, device=dev)
+    guided = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def packed():
+        mf.attn_fwd(q, k, v, plan, out=o, lse=lse, workspace=ws)
+
+    def separate():
+        mf.attn_fwd(qc, kc, vc, plan_c, out=oc, lse=lc, workspace=ws)
+        mf.attn_fwd(qu, ku, vu, plan_u, out=ou, lse=lu, workspace=ws)
+
+    def combine():
+        mf.cfg_combine(o, plan, args.guidance, out=guided)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / args.steps
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    t_packed = timed(packed)
+    t_sep = timed(separate)
+    t_comb = timed(combine)
+    clk = clocks.stop()
+    for p in (plan, plan_c, plan_u):
+        mf.check(p)
+    fwd_flop, _, lens = pack_flops(wl.samples, H, D)
+    line = {"metric": "CFG inference: packed cond+uncond attention forward + guidance, speedup over two "
+                      "separate forwards + guidance",
+            "value": (t_sep + t_comb) / (t_packed + t_comb), "unit": "x", "higher_is_better": True,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{wl.name} seed {wl.seed}", "total_tokens": T, "heads": H, "head_dim": D,
+                       "guidance": args.guidance},
+            "packed_fwd_ms": t_packed, "separate_fwd_ms": t_sep, "combine_ms": t_comb,
+            "packed_fwd_tflops": fwd_flop / (t_packed * 1e-3) / 1e12,
+            "gpu_launches": 2 * args.steps + 4 * args.steps + args.steps,
+            "clocks": clk}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "cfg":
+        return run_cfg(args)
     return run_mf(args)
 
 

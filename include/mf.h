@@ -222,6 +222,22 @@ MF_API mf_status mf_attn_bwd_noalloc(const void *q, const void *k, const void *v
                                      int32_t heads, int32_t head_dim, float softmax_scale,
                                      void *dq, void *dk, void *dv, void *stream);
 
+/* Classifier-free guidance over a pack whose samples come in (conditional,
+ * unconditional) pairs: samples 2p and 2p + 1 are the two branches of prompt
+ * p, run in one packed forward (review, section on CFG).  For the image rows
+ * of each pair (the rows with an image position; they end each sample, so
+ * row j from the end of one pairs with row j from the end of the other):
+ *     out[cond row] = u + guidance * (c - u)
+ * in fp32, rounded to bf16.  The pages do not print the combination; this is
+ * the standard reading.  Other rows of `out` are left untouched, and `out`
+ * may be `o` itself.
+ *   o, out   device bf16 [plan->total_tokens, heads, head_dim]
+ * Errors: as mf_attn_fwd's argument checks, MF_ERR_INVALID_ARG for an odd
+ * sample count or a non-finite guidance; a pair whose image sizes differ is
+ * skipped and mf_check reports MF_ERR_INVALID_ARG. */
+MF_API mf_status mf_cfg_combine(const void *o, const mf_plan *plan, int32_t heads, int32_t head_dim,
+                                float guidance, void *out, void *stream);
+
 /* Synchronize `stream`, then read and clear the plan's device status word:
  * MF_OK, MF_ERR_TIMEOUT, MF_ERR_RANGE, or MF_ERR_CUDA for a failed
  * synchronization. */

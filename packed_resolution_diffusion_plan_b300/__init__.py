@@ -17,7 +17,7 @@ import os
 import torch
 
 __all__ = ["MfError", "Plan", "pack_plan", "attn_fwd", "attn_bwd", "check", "record_main_kernel", "lib",
-           "library_path", "fwd_workspace_bytes", "bwd_workspace_bytes", "debug_inject",
+           "library_path", "fwd_workspace_bytes", "bwd_workspace_bytes", "debug_inject", "cfg_combine",
            "DEBUG_DROP_FWD_KV", "DEBUG_DROP_BWD_QDO", "EXPORTED_SYMBOLS", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -28,7 +28,7 @@ STATUS = {0: "MF_OK", 1: "MF_ERR_INVALID_ARG", 2: "MF_ERR_UNSUPPORTED", 3: "MF_E
 
 EXPORTED_SYMBOLS = ["mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd_workspace_size", "mf_attn_fwd",
                     "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_attn_bwd_noalloc", "mf_check",
-                    "mf_record_main_kernel", "mf_debug_inject",
+                    "mf_record_main_kernel", "mf_debug_inject", "mf_cfg_combine",
                     "mf_status_string", "mf_last_cuda_error"]
 
 TILE = 128
@@ -85,13 +85,14 @@ def lib():
     L.mf_check.argtypes = [ctypes.POINTER(MfPlan), c_vp]
     L.mf_record_main_kernel.argtypes = [c_vp, c_vp]
     L.mf_debug_inject.argtypes = [c_i32]
+    L.mf_cfg_combine.argtypes = [c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32, ctypes.c_float, c_vp, c_vp]
     L.mf_status_string.argtypes = [c_i32]
     L.mf_status_string.restype = ctypes.c_char_p
     L.mf_last_cuda_error.argtypes = []
     L.mf_last_cuda_error.restype = ctypes.c_char_p
     for name in ("mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd_workspace_size", "mf_attn_fwd",
                  "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_record_main_kernel",
-                 "mf_debug_inject"):
+                 "mf_debug_inject", "mf_cfg_combine"):
         getattr(L, name).restype = c_i32
     _lib = L
     return L
@@ -269,6 +270,19 @@ def record_main_kernel(start=None, stop=None, stream=None):
     else:
         a = b = None
     _raise(lib().mf_record_main_kernel(a, b), "mf_record_main_kernel")
+
+
+def cfg_combine(o, plan: Plan, guidance: float, out=None, stream=None):
+    """Classifier-free guidance over (cond, uncond) sample pairs (see
+    mf_cfg_combine): out's conditional image rows = u + guidance (c - u)."""
+    _check_qkv(plan, o)
+    T, H, D = o.shape
+    if out is None:
+        out = o.clone()
+    _check_qkv(plan, out)
+    _raise(lib().mf_cfg_combine(ctypes.c_void_p(o.data_ptr()), ctypes.byref(plan.raw), H, D, float(guidance),
+                                ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream, o.device)), "mf_cfg_combine")
+    return out
 
 
 DEBUG_DROP_FWD_KV = 1

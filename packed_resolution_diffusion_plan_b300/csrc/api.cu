@@ -409,6 +409,7 @@ mf_status mf_check(const mf_plan* plan, void* stream) {
       g_last_cuda_error = "a kernel found its shared memory misaligned and did no work";
       return MF_ERR_CUDA;
     }
+    if (status & mf::kStatusPairing) return MF_ERR_INVALID_ARG;
     return (status & mf::kStatusTimeout) ? MF_ERR_TIMEOUT : MF_ERR_RANGE;
   }
   return MF_OK;
@@ -435,6 +436,19 @@ const char* mf_status_string(mf_status status) {
 }
 
 const char* mf_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+mf_status mf_cfg_combine(const void* o, const mf_plan* plan, int32_t heads, int32_t head_dim, float guidance,
+                         void* out, void* stream) {
+  mf_status st = check_attn_common(plan, heads, head_dim);
+  if (st != MF_OK) return st;
+  if (plan->n_samples % 2 != 0 || !std::isfinite(guidance)) return MF_ERR_INVALID_ARG;
+  if (plan->total_tokens == 0) return MF_OK;
+  if (!o || !out || !aligned16(o) || !aligned16(out)) return MF_ERR_INVALID_ARG;
+  const mf::AttnGeom g = make_geom(plan, heads);
+  cudaError_t e = mf::launch_cfg_combine(o, g, head_dim, guidance, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mf_cfg_combine");
+  return MF_OK;
+}
 
 mf_status mf_debug_inject(int32_t flags) {
   if (flags & ~(MF_DEBUG_DROP_FWD_KV | MF_DEBUG_DROP_BWD_QDO)) return MF_ERR_INVALID_ARG;

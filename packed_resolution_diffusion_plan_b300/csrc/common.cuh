@@ -81,6 +81,11 @@ struct FwdArgs {
   float* lse;                // [heads, T]
 };
 
+// guided = u + g (c - u) on the conditional image rows of each (cond, uncond)
+// sample pair of the pack.
+cudaError_t launch_cfg_combine(const void* o, const AttnGeom& g, int head_dim, float guidance, void* out,
+                               cudaStream_t stream);
+
 // ev_start / ev_stop (may be null) are recorded around the main kernel.
 cudaError_t launch_attn_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, int head_dim, cudaStream_t stream,

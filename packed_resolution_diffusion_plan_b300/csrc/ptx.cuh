@@ -26,6 +26,9 @@ constexpr int kStatusRange = 2;
 // A kernel found its shared-memory window misaligned for the swizzled tiles
 // and did no work.
 constexpr int kStatusLayout = 4;
+// A classifier-free-guidance pair whose two samples have different image
+// sizes (mf_cfg_combine skipped its rows).
+constexpr int kStatusPairing = 8;
 // Largest finite fp16 magnitude: the logit MMA's operands must stay below it.
 constexpr float kF16Max = 65504.0f;
 
