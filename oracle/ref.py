@@ -38,6 +38,15 @@ What it computes, and where each step comes from:
   branches run in one packed forward).  The pages do not print the
   combination; the standard reading is taken: guided = u + g (c - u) for the
   image rows of each pair, written over the conditional sample's image rows.
+* ``norm_modulate``, ``gate_residual``, ``attn_block_fwd`` -- the memory-bound
+  chains around one joint-attention block (review, kernel-fusion section:
+  normalisation, adaptive modulation, RoPE application, gating and the
+  residual add are fused instead of run as separate kernels).  The pages do
+  not give the operations' exact form; the plainest reading of adaptive
+  modulation in a diffusion transformer is taken: y = LN(x) (1 + scale_s) +
+  shift_s with a LayerNorm over the hidden size (no affine, eps 1e-6) and
+  per-sample modulation vectors, and out = x + gate_s * z after the output
+  projection.  The projections are plain matrix products (synthetic weights).
 * ``brute_force_masked`` -- the thing the offsets replace: dense attention
   over the whole pack with an explicit block-diagonal mask.  Written
   separately from ``attn_fwd`` on purpose.
@@ -316,6 +325,48 @@ def cfg_combine(o, cu_seqlens, pos, guidance: float):
         for rc, ru in zip(c_img, u_img):
             out[rc] = o[ru] + guidance * (o[rc] - o[ru])
     return out
+
+
+def _sample_of_token(cu_seqlens):
+    cu = np.asarray(cu_seqlens)
+    return np.repeat(np.arange(len(cu) - 1), np.diff(cu))
+
+
+def norm_modulate(x, cu_seqlens, shift, scale, eps: float = 1e-6):
+    """y = LN(x) * (1 + scale_s) + shift_s for every token of sample s.
+
+    x [T, C]; shift, scale [n_samples, C].  LN normalises each row over C to
+    zero mean and unit variance (population variance, eps inside the square
+    root), without a learned affine.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    s = _sample_of_token(cu_seqlens)
+    mu = x.mean(axis=1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=1, keepdims=True)
+    n = (x - mu) / np.sqrt(var + eps)
+    return n * (1.0 + np.asarray(scale, dtype=np.float64)[s]) + np.asarray(shift, dtype=np.float64)[s]
+
+
+def gate_residual(x, z, cu_seqlens, gate):
+    """out = x + gate_s * z for every token of sample s (x, z [T, C])."""
+    s = _sample_of_token(cu_seqlens)
+    return np.asarray(x, dtype=np.float64) + np.asarray(gate, dtype=np.float64)[s] * np.asarray(z, dtype=np.float64)
+
+
+def attn_block_fwd(x, cu_seqlens, pos, heads: int, w_qkv, w_o, shift, scale, gate, softmax_scale: float = 0.0,
+                   eps: float = 1e-6, frame=None, rope_axes: int = 2):
+    """One joint-attention block: x + gate * (Attn(R(q), R(k), v) W_o) with
+    [q | k | v] = norm_modulate(x) W_qkv; x [T, C], W_qkv [C, 3C], W_o [C, C],
+    C = heads * head_dim, the columns of each third ordered [head][dim]."""
+    x = np.asarray(x, dtype=np.float64)
+    T, C = x.shape
+    D = C // heads
+    y = norm_modulate(x, cu_seqlens, shift, scale, eps)
+    qkv = y @ np.asarray(w_qkv, dtype=np.float64)
+    q, k, v = (qkv[:, i * C:(i + 1) * C].reshape(T, heads, D) for i in range(3))
+    O, _ = attn_fwd(q, k, v, cu_seqlens, pos, softmax_scale, frame=frame, rope_axes=rope_axes)
+    z = O.reshape(T, C) @ np.asarray(w_o, dtype=np.float64)
+    return gate_residual(x, z, cu_seqlens, gate)
 
 
 def brute_force_masked(q, k, v, cu_seqlens, pos, softmax_scale: float = 0.0,

@@ -314,6 +314,70 @@ def test_cfg_combine_closed_forms():
 
 
 # --------------------------------------------------------------------------
+# the memory-bound chains around a joint-attention block
+# --------------------------------------------------------------------------
+
+def test_norm_modulate_closed_form_and_library():
+    """Hand-derived: x = (1, 3) has mean 2 and variance 1, so LN(x) =
+    (-1, 1)/sqrt(1 + eps); modulation scales by 1 + scale and shifts.  The
+    normalisation also matches torch's layer_norm in float64 (a library
+    routine), and each token takes its own sample's vectors."""
+    eps = 1e-6
+    cu = np.array([0, 1, 3])
+    x = np.array([[1.0, 3.0], [0.0, 4.0], [2.0, -2.0]])
+    shift = np.array([[0.25, -0.5], [1.0, 2.0]])
+    scale = np.array([[0.5, 0.0], [-1.0, 3.0]])
+    y = oracle.norm_modulate(x, cu, shift, scale, eps)
+    r = 1.0 / math.sqrt(1.0 + eps)
+    assert np.allclose(y[0], [-r * 1.5 + 0.25, r * 1.0 - 0.5], atol=1e-15)
+    r4 = 2.0 / math.sqrt(4.0 + eps)
+    assert np.allclose(y[1], [-r4 * 0.0 + 1.0, r4 * 4.0 + 2.0], atol=1e-15)
+    rng = np.random.default_rng(9)
+    xr = rng.standard_normal((7, 64)) * 3 + 1
+    zero = np.zeros((1, 64))
+    ln = torch.nn.functional.layer_norm(torch.from_numpy(xr), (64,), eps=eps).numpy()
+    assert np.allclose(oracle.norm_modulate(xr, np.array([0, 7]), zero, zero, eps), ln, atol=1e-12)
+
+
+def test_gate_residual_closed_form():
+    cu = np.array([0, 2, 3])
+    x = np.arange(6.0).reshape(3, 2)
+    z = np.ones((3, 2))
+    gate = np.array([[2.0, -1.0], [0.5, 0.0]])
+    out = oracle.gate_residual(x, z, cu, gate)
+    assert np.array_equal(out, np.array([[2.0, 0.0], [4.0, 2.0], [4.5, 5.0]]))
+
+
+def test_attn_block_closed_forms():
+    """gate 0 leaves x unchanged; with zero Q/K weights every logit is 0, the
+    attention of a sample is the mean of its v rows, and the block reduces to
+    x + gate * mean_s(v) W_o in closed form."""
+    rng = np.random.default_rng(10)
+    heads, D = 2, 8
+    C = heads * D
+    samples = [(3, 32, 16), (2, 16, 16)]
+    p = oracle.pack_plan(samples)
+    T = p["total_tokens"]
+    cu = p["cu_seqlens"]
+    x = rng.standard_normal((T, C))
+    w_qkv = rng.standard_normal((C, 3 * C)) / math.sqrt(C)
+    w_o = rng.standard_normal((C, C)) / math.sqrt(C)
+    shift, scale, gate = (rng.standard_normal((2, C)) * 0.1 for _ in range(3))
+    out0 = oracle.attn_block_fwd(x, cu, p["pos"], heads, w_qkv, w_o, shift, scale, np.zeros((2, C)))
+    assert np.array_equal(out0, x)
+    w_v = w_qkv.copy()
+    w_v[:, :2 * C] = 0.0
+    out = oracle.attn_block_fwd(x, cu, p["pos"], heads, w_v, w_o, shift, scale, gate)
+    y = oracle.norm_modulate(x, cu, shift, scale)
+    v = y @ w_v[:, 2 * C:]
+    want = x.copy()
+    for i in range(2):
+        a, b = int(cu[i]), int(cu[i + 1])
+        want[a:b] += gate[i] * (v[a:b].mean(axis=0) @ w_o)
+    assert np.allclose(out, want, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
 # forward
 # --------------------------------------------------------------------------
 
