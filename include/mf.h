@@ -222,6 +222,44 @@ MF_API mf_status mf_attn_bwd_noalloc(const void *q, const void *k, const void *v
                                      int32_t heads, int32_t head_dim, float softmax_scale,
                                      void *dq, void *dk, void *dv, void *stream);
 
+/* The memory-bound chains around one joint-attention block, each one fused
+ * pass over HBM (review, kernel-fusion section: normalisation, adaptive
+ * modulation, RoPE application, gating and the residual add run fused
+ * instead of as separate kernels).  The pages give no exact form; the
+ * plainest reading for a diffusion-transformer block is used.  The
+ * projections around them are plain matrix products left to the caller
+ * (e.g. cuBLAS):
+ *     y   = mf_norm_modulate(x)               LN(x) (1 + scale_s) + shift_s
+ *     qkv = y W_qkv                           [q | k | v], each [heads, head_dim]
+ *     o   = mf_attn_fwd_qkv(qkv)              RoPE fused into its first pass
+ *     z   = o W_o
+ *     out = mf_gate_residual(x, z)            x + gate_s * z
+ * Modulation vectors are per sample of the plan (s = the sample a token
+ * belongs to), bf16 [n_samples, hidden]; x, y, z, out are bf16
+ * [total_tokens, hidden], 16-byte aligned.
+ *
+ * mf_norm_modulate: LayerNorm over the hidden size without affine (mean and
+ * population variance of the row, eps inside the square root, fp32), then
+ * the modulation, rounded to bf16.  hidden in {1024, 2048, 3072, 4096, 6144,
+ * 8192} (else MF_ERR_UNSUPPORTED). */
+MF_API mf_status mf_norm_modulate(const void *x, const mf_plan *plan, int32_t hidden, const void *shift,
+                                  const void *scale, float eps, void *y, void *stream);
+
+/* out = x + gate_s * z in fp32, rounded to bf16 (hidden a multiple of 8;
+ * out may be x). */
+MF_API mf_status mf_gate_residual(const void *x, const void *z, const mf_plan *plan, int32_t hidden,
+                                  const void *gate, void *out, void *stream);
+
+/* mf_attn_fwd on the output of a QKV projection: qkv is bf16
+ * [total_tokens, 3 * heads * head_dim], each row [q | k | v] with every
+ * third ordered [head][dim].  The first pass reads q and k from those rows
+ * and rotates them into the workspace (so the split and the RoPE cost no
+ * extra pass), and the attention kernel reads v in place.  Workspace, o, lse
+ * and errors as mf_attn_fwd. */
+MF_API mf_status mf_attn_fwd_qkv(const void *qkv, const mf_plan *plan, int32_t heads, int32_t head_dim,
+                                 float softmax_scale, void *workspace, size_t workspace_bytes, void *o,
+                                 float *lse, void *stream);
+
 /* Classifier-free guidance over a pack whose samples come in (conditional,
  * unconditional) pairs: samples 2p and 2p + 1 are the two branches of prompt
  * p, run in one packed forward (review, section on CFG).  For the image rows

@@ -17,7 +17,7 @@ import os
 import torch
 
 __all__ = ["MfError", "Plan", "pack_plan", "attn_fwd", "attn_bwd", "check", "record_main_kernel", "lib",
-           "library_path", "fwd_workspace_bytes", "bwd_workspace_bytes", "debug_inject", "cfg_combine",
+           "library_path", "fwd_workspace_bytes", "bwd_workspace_bytes", "debug_inject", "cfg_combine", "norm_modulate", "gate_residual", "attn_fwd_qkv",
            "DEBUG_DROP_FWD_KV", "DEBUG_DROP_BWD_QDO", "EXPORTED_SYMBOLS", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -28,7 +28,8 @@ STATUS = {0: "MF_OK", 1: "MF_ERR_INVALID_ARG", 2: "MF_ERR_UNSUPPORTED", 3: "MF_E
 
 EXPORTED_SYMBOLS = ["mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd_workspace_size", "mf_attn_fwd",
                     "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_attn_bwd_noalloc", "mf_check",
-                    "mf_record_main_kernel", "mf_debug_inject", "mf_cfg_combine",
+                    "mf_record_main_kernel", "mf_debug_inject", "mf_cfg_combine", "mf_norm_modulate",
+                    "mf_gate_residual", "mf_attn_fwd_qkv",
                     "mf_status_string", "mf_last_cuda_error"]
 
 TILE = 128
@@ -86,13 +87,17 @@ def lib():
     L.mf_record_main_kernel.argtypes = [c_vp, c_vp]
     L.mf_debug_inject.argtypes = [c_i32]
     L.mf_cfg_combine.argtypes = [c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32, ctypes.c_float, c_vp, c_vp]
+    L.mf_norm_modulate.argtypes = [c_vp, ctypes.POINTER(MfPlan), c_i32, c_vp, c_vp, ctypes.c_float, c_vp, c_vp]
+    L.mf_gate_residual.argtypes = [c_vp, c_vp, ctypes.POINTER(MfPlan), c_i32, c_vp, c_vp, c_vp]
+    L.mf_attn_fwd_qkv.argtypes = [c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32, ctypes.c_float, c_vp, c_sz, c_vp,
+                                  c_vp, c_vp]
     L.mf_status_string.argtypes = [c_i32]
     L.mf_status_string.restype = ctypes.c_char_p
     L.mf_last_cuda_error.argtypes = []
     L.mf_last_cuda_error.restype = ctypes.c_char_p
     for name in ("mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd_workspace_size", "mf_attn_fwd",
                  "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_record_main_kernel",
-                 "mf_debug_inject", "mf_cfg_combine"):
+                 "mf_debug_inject", "mf_cfg_combine", "mf_norm_modulate", "mf_gate_residual", "mf_attn_fwd_qkv"):
         getattr(L, name).restype = c_i32
     _lib = L
     return L
@@ -270,6 +275,57 @@ def record_main_kernel(start=None, stop=None, stream=None):
     else:
         a = b = None
     _raise(lib().mf_record_main_kernel(a, b), "mf_record_main_kernel")
+
+
+def _check_rows(plan: Plan, *ts):
+    for t in ts:
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError("expected contiguous bf16 CUDA tensors [rows, hidden]")
+
+
+def norm_modulate(x, plan: Plan, shift, scale, eps: float = 1e-6, out=None, stream=None):
+    """LN(x) (1 + scale_s) + shift_s per sample s (see mf_norm_modulate)."""
+    _check_rows(plan, x, shift, scale)
+    T, C = x.shape
+    if T != plan.total_tokens or shift.shape != (plan.n_samples, C) or scale.shape != shift.shape:
+        raise ValueError("x is [total_tokens, hidden], shift/scale are [n_samples, hidden]")
+    out = torch.empty_like(x) if out is None else out
+    _raise(lib().mf_norm_modulate(ctypes.c_void_p(x.data_ptr()), ctypes.byref(plan.raw), C,
+                                  ctypes.c_void_p(shift.data_ptr()), ctypes.c_void_p(scale.data_ptr()), float(eps),
+                                  ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream, x.device)), "mf_norm_modulate")
+    return out
+
+
+def gate_residual(x, z, plan: Plan, gate, out=None, stream=None):
+    """x + gate_s * z per sample s (see mf_gate_residual)."""
+    _check_rows(plan, x, z, gate)
+    T, C = x.shape
+    if z.shape != x.shape or T != plan.total_tokens or gate.shape != (plan.n_samples, C):
+        raise ValueError("x, z are [total_tokens, hidden], gate is [n_samples, hidden]")
+    out = torch.empty_like(x) if out is None else out
+    _raise(lib().mf_gate_residual(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(z.data_ptr()), ctypes.byref(plan.raw),
+                                  C, ctypes.c_void_p(gate.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                  _stream_ptr(stream, x.device)), "mf_gate_residual")
+    return out
+
+
+def attn_fwd_qkv(qkv, plan: Plan, heads: int, softmax_scale: float = 0.0, out=None, lse=None, workspace=None,
+                 stream=None):
+    """O, LSE from a QKV projection's output [T, 3 * heads * head_dim] (see mf_attn_fwd_qkv)."""
+    _check_rows(plan, qkv)
+    T, C3 = qkv.shape
+    D = plan.head_dim
+    if T != plan.total_tokens or C3 != 3 * heads * D:
+        raise ValueError(f"expected [{plan.total_tokens}, {3 * heads * D}], got {tuple(qkv.shape)}")
+    out = torch.empty((T, heads, D), dtype=torch.bfloat16, device=qkv.device) if out is None else out
+    lse = torch.empty((heads, T), dtype=torch.float32, device=qkv.device) if lse is None else lse
+    if workspace is None:
+        workspace = torch.empty(max(256, fwd_workspace_bytes(T, heads, D)), dtype=torch.uint8, device=qkv.device)
+    _raise(lib().mf_attn_fwd_qkv(ctypes.c_void_p(qkv.data_ptr()), ctypes.byref(plan.raw), heads, D,
+                                 float(softmax_scale), ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                 ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+                                 _stream_ptr(stream, qkv.device)), "mf_attn_fwd_qkv")
+    return out, lse
 
 
 def cfg_combine(o, plan: Plan, guidance: float, out=None, stream=None):

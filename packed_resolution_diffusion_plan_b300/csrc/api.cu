@@ -124,7 +124,8 @@ EncodeTiledFn encode_fn() {
 // [rows, heads*head_dim] view of a [T, heads, head_dim] tensor of 16-bit
 // elements; boxes of 128 rows x 64 columns, 128-byte swizzle, zero fill past
 // the last row.
-mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t heads, int32_t head_dim) {
+mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t heads, int32_t head_dim,
+                    int64_t row_elems = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     g_last_cuda_error = "cuTensorMapEncodeTiled entry point not available";
@@ -132,7 +133,9 @@ mf_status make_tmap(CUtensorMap* map, const void* base, int32_t rows, int32_t he
   }
   const cuuint64_t cols = static_cast<cuuint64_t>(heads) * head_dim;
   cuuint64_t gdim[2] = {cols, static_cast<cuuint64_t>(rows)};
-  cuuint64_t gstride[1] = {cols * 2};
+  // row_elems: elements from one token's row to the next (0 = cols, a plain
+  // [T, heads, head_dim] tensor; 3 cols for the V third of a QKV projection)
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(row_elems > 0 ? row_elems : static_cast<int64_t>(cols)) * 2};
   cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mf::kTile)};
   cuuint32_t estride[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
@@ -293,9 +296,16 @@ mf_status mf_attn_fwd_workspace_size(int32_t total_tokens, int32_t heads, int32_
   return MF_OK;
 }
 
-mf_status mf_attn_fwd(const void* q, const void* k, const void* v, const mf_plan* plan, int32_t heads,
-                      int32_t head_dim, float softmax_scale, void* workspace, size_t workspace_bytes, void* o,
-                      float* lse, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward over q, k, v whose token rows are `stride` elements apart
+// (heads * head_dim for plain tensors, 3 heads * head_dim for the thirds of a
+// QKV projection).
+mf_status attn_fwd_impl(const void* q, const void* k, const void* v, int64_t stride, const mf_plan* plan,
+                        int32_t heads, int32_t head_dim, float softmax_scale, void* workspace,
+                        size_t workspace_bytes, void* o, float* lse, void* stream, const char* who) {
   mf_status st = check_attn_common(plan, heads, head_dim);
   if (st != MF_OK) return st;
   if (plan->total_tokens == 0) return MF_OK;
@@ -314,6 +324,7 @@ mf_status mf_attn_fwd(const void* q, const void* k, const void* v, const mf_plan
   a.scale_log2 = resolve_scale(softmax_scale, head_dim) * kLog2e;
   a.q = q;
   a.k = k;
+  a.qk_stride = stride;
   a.q_rot = ws;
   a.k_rot = ws + align_up(rows * head_dim * 2, 256);
   a.o = o;
@@ -322,12 +333,33 @@ mf_status mf_attn_fwd(const void* q, const void* k, const void* v, const mf_plan
   CUtensorMap tq, tk, tv;
   if ((st = make_tmap(&tq, a.q_rot, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   if ((st = make_tmap(&tk, a.k_rot, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
-  if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim, stride)) != MF_OK) return st;
   cudaEvent_t ev0, ev1;
   take_events(&ev0, &ev1);
   cudaError_t e = mf::launch_attn_fwd(a, tq, tk, tv, head_dim, static_cast<cudaStream_t>(stream), ev0, ev1);
-  if (e != cudaSuccess) return cuda_fail(e, "mf_attn_fwd");
+  if (e != cudaSuccess) return cuda_fail(e, who);
   return MF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mf_status mf_attn_fwd(const void* q, const void* k, const void* v, const mf_plan* plan, int32_t heads,
+                      int32_t head_dim, float softmax_scale, void* workspace, size_t workspace_bytes, void* o,
+                      float* lse, void* stream) {
+  return attn_fwd_impl(q, k, v, static_cast<int64_t>(heads) * head_dim, plan, heads, head_dim, softmax_scale,
+                       workspace, workspace_bytes, o, lse, stream, "mf_attn_fwd");
+}
+
+mf_status mf_attn_fwd_qkv(const void* qkv, const mf_plan* plan, int32_t heads, int32_t head_dim,
+                          float softmax_scale, void* workspace, size_t workspace_bytes, void* o, float* lse,
+                          void* stream) {
+  if (qkv == nullptr || heads < 1) return MF_ERR_INVALID_ARG;
+  const int64_t C = static_cast<int64_t>(heads) * head_dim;
+  const uint8_t* base = static_cast<const uint8_t*>(qkv);
+  return attn_fwd_impl(base, base + C * 2, base + 2 * C * 2, 3 * C, plan, heads, head_dim, softmax_scale,
+                       workspace, workspace_bytes, o, lse, stream, "mf_attn_fwd_qkv");
 }
 
 mf_status mf_attn_bwd_workspace_size(int32_t total_tokens, int32_t heads, int32_t head_dim, size_t* bytes) {
@@ -447,6 +479,44 @@ mf_status mf_cfg_combine(const void* o, const mf_plan* plan, int32_t heads, int3
   const mf::AttnGeom g = make_geom(plan, heads);
   cudaError_t e = mf::launch_cfg_combine(o, g, head_dim, guidance, out, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mf_cfg_combine");
+  return MF_OK;
+}
+
+// Plan checks shared by the chain calls (they read only the offsets).
+mf_status check_chain(const mf_plan* plan, int32_t hidden) {
+  if (plan == nullptr || hidden <= 0) return MF_ERR_INVALID_ARG;
+  if (plan->total_tokens < 0 || plan->n_samples < 0) return MF_ERR_INVALID_ARG;
+  if (plan->total_tokens > 0 && plan->cu_seqlens == nullptr) return MF_ERR_INVALID_ARG;
+  return MF_OK;
+}
+
+mf_status mf_norm_modulate(const void* x, const mf_plan* plan, int32_t hidden, const void* shift,
+                           const void* scale, float eps, void* y, void* stream) {
+  mf_status st = check_chain(plan, hidden);
+  if (st != MF_OK) return st;
+  const int k = hidden / 1024;
+  if (hidden % 1024 != 0 || !(k == 1 || k == 2 || k == 3 || k == 4 || k == 6 || k == 8)) return MF_ERR_UNSUPPORTED;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return MF_ERR_INVALID_ARG;
+  if (plan->total_tokens == 0) return MF_OK;
+  if (!x || !shift || !scale || !y) return MF_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(shift) || !aligned16(scale) || !aligned16(y)) return MF_ERR_INVALID_ARG;
+  mf::AttnGeom g = make_geom(plan, 1);
+  cudaError_t e = mf::launch_norm_modulate(x, g, hidden, shift, scale, eps, y, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mf_norm_modulate");
+  return MF_OK;
+}
+
+mf_status mf_gate_residual(const void* x, const void* z, const mf_plan* plan, int32_t hidden, const void* gate,
+                           void* out, void* stream) {
+  mf_status st = check_chain(plan, hidden);
+  if (st != MF_OK) return st;
+  if (hidden % 8 != 0) return MF_ERR_UNSUPPORTED;
+  if (plan->total_tokens == 0) return MF_OK;
+  if (!x || !z || !gate || !out) return MF_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(z) || !aligned16(gate) || !aligned16(out)) return MF_ERR_INVALID_ARG;
+  mf::AttnGeom g = make_geom(plan, 1);
+  cudaError_t e = mf::launch_gate_residual(x, z, g, hidden, gate, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mf_gate_residual");
   return MF_OK;
 }
 

@@ -79,8 +79,10 @@ __global__ void fwd_pre_kernel(const FwdArgs a) {
   if (gid >= rows * kChunks) return;
   const long long tok = gid / kChunks / a.g.heads;
   const int ch = static_cast<int>(gid % kChunks);
-  const uint4 qv = reinterpret_cast<const uint4*>(a.q)[gid];
-  const uint4 kv = reinterpret_cast<const uint4*>(a.k)[gid];
+  // q, k rows are qk_stride elements apart (a plain tensor or a QKV row)
+  const long long src = (tok * a.qk_stride + (gid / kChunks % a.g.heads) * D) / 8 + ch;
+  const uint4 qv = reinterpret_cast<const uint4*>(a.q)[src];
+  const uint4 kv = reinterpret_cast<const uint4*>(a.k)[src];
   const uint32_t* qw = reinterpret_cast<const uint32_t*>(&qv);
   const uint32_t* kw = reinterpret_cast<const uint32_t*>(&kv);
   const int2 p = reinterpret_cast<const int2*>(a.g.pos)[tok];

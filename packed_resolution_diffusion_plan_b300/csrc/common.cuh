@@ -73,13 +73,20 @@ struct AttnGeom {
 struct FwdArgs {
   AttnGeom g;
   float scale_log2;          // softmax_scale * log2(e), folded into the fp16 Q operand
-  const void* q;             // bf16 [T, heads, D]
+  const void* q;             // bf16, token rows qk_stride elements apart, [heads, D] each
   const void* k;
+  int64_t qk_stride;         // heads * D, or 3 heads * D for a QKV projection's rows
   void* q_rot;               // fp16 [T, heads, D] s log2(e) R(q)
   void* k_rot;               // fp16 [T, heads, D] R(k)
   void* o;                   // bf16 [T, heads, D]
   float* lse;                // [heads, T]
 };
+
+// The memory-bound chains around a joint-attention block (chain.cu).
+cudaError_t launch_norm_modulate(const void* x, const AttnGeom& g, int hidden, const void* shift, const void* scale,
+                                 float eps, void* y, cudaStream_t stream);
+cudaError_t launch_gate_residual(const void* x, const void* z, const AttnGeom& g, int hidden, const void* gate,
+                                 void* out, cudaStream_t stream);
 
 // guided = u + g (c - u) on the conditional image rows of each (cond, uncond)
 // sample pair of the pack.

@@ -123,6 +123,16 @@ def test_attn_validation_without_gpu(L):
     empty.head_dim, empty.rope_axes = 128, 2
     assert L.mf_attn_fwd(None, None, None, ctypes.byref(empty), 2, 128, 0.0, None, 0, None, None, None) == 0
     assert L.mf_check(None, None) == 1
+    # the chain calls: unsupported hidden sizes, null pointers, bad eps
+    assert L.mf_norm_modulate(ok, ctypes.byref(plan), 1000, ok, ok, 1e-6, ok, None) == 2
+    assert L.mf_norm_modulate(ok, ctypes.byref(plan), 3072, None, ok, 1e-6, ok, None) == 1
+    assert L.mf_norm_modulate(ok, ctypes.byref(plan), 3072, ok, ok, -1.0, ok, None) == 1
+    assert L.mf_norm_modulate(ok, None, 3072, ok, ok, 1e-6, ok, None) == 1
+    assert L.mf_gate_residual(ok, ok, ctypes.byref(plan), 12, ok, ok, None) == 2
+    assert L.mf_gate_residual(ok, None, ctypes.byref(plan), 16, ok, ok, None) == 1
+    assert L.mf_attn_fwd_qkv(None, ctypes.byref(plan), 2, 128, 0.0, ok, big, ok, ok, None) == 1
+    assert L.mf_attn_fwd_qkv(ok, ctypes.byref(plan), 2, 96, 0.0, ok, big, ok, ok, None) == 2
+    assert L.mf_cfg_combine(ok, ctypes.byref(plan), 2, 128, 1.0, ok, None) == 1   # odd sample count
     # the timeout-path test aid takes only the documented bits
     assert L.mf_debug_inject(4) == 1 and L.mf_debug_inject(-1) == 1
     assert L.mf_debug_inject(3) == 0 and L.mf_debug_inject(0) == 0
