@@ -45,9 +45,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mf", "reference"], default="mf")
-    ap.add_argument("--mode", choices=["step", "cfg"], default="step",
+    ap.add_argument("--mode", choices=["step", "cfg", "chain"], default="step",
                     help="step: the fwd+bwd training step (the headline); cfg: the CFG pair pack's "
-                         "packed forward + guidance against two separate forwards")
+                         "packed forward + guidance against two separate forwards; chain: one attention "
+                         "block's memory-bound chains fused against unfused")
     ap.add_argument("--guidance", type=float, default=4.0)
     ap.add_argument("--workload", default="native_res_32k", choices=list(synth.WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
@@ -517,12 +518,119 @@ def run_cfg(args):
     return 0
 
 
+def run_chain(args):
+    """One joint-attention block forward on a pack (synthetic weights, hidden =
+    heads * head_dim): x -> LN + modulation -> @W_qkv -> attention -> @W_o ->
+    gate + residual.  Fused: mf_norm_modulate, mf_attn_fwd_qkv (split + RoPE in
+    its first pass), mf_gate_residual.  Unfused: the same operations as
+    separate torch kernels (layer_norm, gather of the per-sample vectors, mul,
+    add, contiguous q/k/v copies, mf_attn_fwd, mul, add).  Both use the same
+    cuBLAS products and the same attention kernel; the JSON line reports each
+    part and the memory-bound chains' total both ways."""
+    import packed_resolution_diffusion_plan_b300 as mf
+    dev = torch.device("cuda", 0)
+    wl = synth.WORKLOADS[args.workload](args.seed)
+    H, D = wl.heads, wl.head_dim
+    C = H * D
+    plan = mf.pack_plan(wl.samples, token_budget=wl.token_budget, head_dim=D, device=dev, rope_axes=wl.rope_axes)
+    T, n = plan.total_tokens, plan.n_samples
+    g = torch.Generator("cpu").manual_seed(args.seed)
+
+    def rnd(*shape, scale=1.0):
+        return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16).to(dev)
+
+    x = rnd(T, C)
+    w_qkv, w_o = rnd(C, 3 * C, scale=C ** -0.5), rnd(C, C, scale=C ** -0.5)
+    shift, scale, gate = rnd(n, C, scale=0.2), rnd(n, C, scale=0.2), rnd(n, C, scale=0.5)
+    sample_of = torch.repeat_interleave(torch.arange(n, device=dev), torch.diff(plan.cu_seqlens().long()))
+    ws = torch.empty(mf.fwd_workspace_bytes(T, H, D), dtype=torch.uint8, device=dev)
+    y, z, out = torch.empty_like(x), torch.empty((T, C), dtype=torch.bfloat16, device=dev), torch.empty_like(x)
+    qkv = torch.empty((T, 3 * C), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = {}
+
+    def mark(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        ev.setdefault(name, []).append(e)
+
+    def fused():
+        mark("f0"); mf.norm_modulate(x, plan, shift, scale, out=y)
+        mark("f1"); torch.matmul(y, w_qkv, out=qkv)
+        mark("f2"); mf.record_main_kernel(*main_ev["f"]); mf.attn_fwd_qkv(qkv, plan, H, out=o, lse=lse, workspace=ws)
+        mark("f3"); torch.matmul(o.view(T, C), w_o, out=z)
+        mark("f4"); mf.gate_residual(x, z, plan, gate, out=out)
+        mark("f5")
+
+    def unfused():
+        mark("u0")
+        yn = torch.nn.functional.layer_norm(x, (C,), eps=1e-6)
+        yu = yn * (1 + scale.index_select(0, sample_of)) + shift.index_select(0, sample_of)
+        mark("u1"); q3 = torch.matmul(yu, w_qkv)
+        mark("u2")
+        q, k, v = (q3[:, i * C:(i + 1) * C].contiguous().view(T, H, D) for i in range(3))
+        mf.record_main_kernel(*main_ev["u"]); mf.attn_fwd(q, k, v, plan, out=o, lse=lse, workspace=ws)
+        mark("u3"); zz = torch.matmul(o.view(T, C), w_o)
+        mark("u4"); _ = x + gate.index_select(0, sample_of) * zz
+        mark("u5")
+
+    main_ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in "fu"}
+    for _ in range(max(args.warmup, 3)):
+        fused(); unfused()
+    torch.cuda.synchronize(dev)
+    ev.clear()
+    mains = {"f": [], "u": []}
+    clocks = ClockSampler(dev)
+    clocks.start()
+    for _ in range(args.steps):
+        fused(); unfused()
+        torch.cuda.synchronize(dev)
+        for k2 in "fu":
+            mains[k2].append(main_ev[k2][0].elapsed_time(main_ev[k2][1]))
+    clk = clocks.stop()
+    mf.check(plan)
+
+    def span(a, b):
+        return float(np.median([ea.elapsed_time(eb) for ea, eb in zip(ev[a], ev[b])]))
+
+    f = {"norm_modulate": span("f0", "f1"), "qkv_gemm": span("f1", "f2"), "attention": span("f2", "f3"),
+         "out_gemm": span("f3", "f4"), "gate_residual": span("f4", "f5")}
+    u = {"norm_modulate": span("u0", "u1"), "qkv_gemm": span("u1", "u2"), "attention": span("u2", "u3"),
+         "out_gemm": span("u3", "u4"), "gate_residual": span("u4", "u5")}
+    fm, um = float(np.median(mains["f"])), float(np.median(mains["u"]))
+    # memory-bound chains: everything but the two products and the attention main kernel
+    f_chain = f["norm_modulate"] + (f["attention"] - fm) + f["gate_residual"]
+    u_chain = u["norm_modulate"] + (u["attention"] - um) + u["gate_residual"]
+    f_block, u_block = sum(f.values()), sum(u.values())
+    line = {"metric": "joint-attention block forward: fused memory-bound chains (norm + modulation, QKV split + "
+                      "RoPE, gate + residual) against the same operations unfused",
+            "value": u_chain / f_chain, "unit": "x (chain time, unfused / fused)", "higher_is_better": True,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
+            "data": "synthetic (random weights)",
+            "config": {"workload": f"{wl.name} seed {wl.seed}", "total_tokens": T, "hidden": C, "heads": H,
+                       "head_dim": D},
+            "fused_ms": {k2: round(v2, 4) for k2, v2 in f.items()},
+            "unfused_ms": {k2: round(v2, 4) for k2, v2 in u.items()},
+            "attention_main_kernel_ms": round(fm, 4),
+            "chain_ms": {"fused": round(f_chain, 4), "unfused": round(u_chain, 4)},
+            "block_ms": {"fused": round(f_block, 4), "unfused": round(u_block, 4)},
+            "block_speedup": u_block / f_block,
+            "chain_hbm_gbs_fused": (2 * T * C * 2 + (2 * T * C * 2 + 2 * T * C * 2) + 3 * T * C * 2) / (f_chain * 1e-3) / 1e9,
+            "clocks": clk}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.mode == "cfg":
         return run_cfg(args)
+    if args.mode == "chain":
+        return run_chain(args)
     return run_mf(args)
 
 
