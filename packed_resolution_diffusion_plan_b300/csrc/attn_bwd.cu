@@ -176,10 +176,27 @@ __global__ void bwd_dq_kernel(const BwdArgs a) {
   const int fr = a.g.frame[tok];
   uint32_t out[4];
   if (p.x >= 0) {
+    float cs[8];
+    if (a.g.rope_axes == 2) {
+      // 2 axes: the chunk's 4 pairs are consecutive frequencies of one half
+      const int dim0 = ch * 8;
+      const int k0 = (dim0 % (D / 2)) / 2;
+      const int pp = dim0 >= D / 2 ? p.y : p.x;
+      const float4* tab = reinterpret_cast<const float4*>(a.g.rope_cs) + static_cast<size_t>(pp) * (D / 8) + k0 / 2;
+      const float4 c0 = __ldg(tab), c1 = __ldg(tab + 1);
+      cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
+      cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 c = rope_pair_cs<D>(a.g, 4 * ch + e, p, fr);
+        cs[2 * e] = c.x;
+        cs[2 * e + 1] = c.y;
+      }
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 cs = rope_pair_cs<D>(a.g, 4 * ch + e, p, fr);
-      const float c = cs.x, s = cs.y;
+      const float c = cs[2 * e], s = cs[2 * e + 1];
       const float u0 = x[2 * e] * kLn2, u1 = x[2 * e + 1] * kLn2;
       out[e] = pack_bf16(fmaf(u0, c, u1 * s), fmaf(-u0, s, u1 * c));
     }
@@ -198,8 +215,25 @@ template <int D>
 __device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32_t (&v)[32], int col0, float mult,
                                                 int2 p, int f, const AttnGeom& g, bool inverse_rope) {
   uint32_t packed[16];
-  if (inverse_rope && p.x >= 0) {
+  if (inverse_rope && p.x >= 0 && g.rope_axes == 2) {
+    // 2 axes: the chunk's 16 pairs are consecutive frequencies of one half,
+    // read two pairs per 16-byte load
+    const int k0 = (col0 % (D / 2)) / 2;
+    const int pp = col0 >= D / 2 ? p.y : p.x;
+    const float4* tab = reinterpret_cast<const float4*>(g.rope_cs) + static_cast<size_t>(pp) * (D / 8) + k0 / 2;
 #pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 cs = __ldg(tab + q);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float c = e ? cs.z : cs.x, s = e ? cs.w : cs.y;
+        const int m = 2 * q + e;
+        const float u0 = __uint_as_float(v[2 * m]) * mult, u1 = __uint_as_float(v[2 * m + 1]) * mult;
+        packed[m] = pack_bf16(fmaf(u0, c, u1 * s), fmaf(-u0, s, u1 * c));
+      }
+    }
+  } else if (inverse_rope && p.x >= 0) {
+#pragma unroll 4
     for (int m = 0; m < 16; ++m) {
       const float2 cs = rope_pair_cs<D>(g, col0 / 2 + m, p, f);
       const float c = cs.x, s = cs.y;
