@@ -75,7 +75,8 @@ typedef enum {
 } mf_status;
 
 /* One sample of a pack: text length in tokens, image height and width in
- * pixels (positive multiples of 16), and its latent frames: 1 (or 0) for a
+ * pixels (positive multiples of 16, or both 0 for a text-only sample with
+ * text_len > 0), and its latent frames: 1 (or 0) for a
  * generation sample, 2 for an edit sample, whose source and target latents
  * (the same size) follow its text as frames 0 and 1 (review, editing-model
  * section: (h, w, f) positions tell source tokens from target tokens). */
@@ -141,7 +142,8 @@ MF_API mf_status mf_pack_plan_workspace_size(const mf_sample *samples, int32_t n
  * Runs a device prefix scan, the per-token id expansion and the RoPE table on
  * `stream`, then synchronizes `stream` once to read the scalars back.
  * Errors: MF_ERR_INVALID_ARG (null pointer, text_len < 0, H or W not a
- * positive multiple of 16, frames not in {0, 1, 2}, frames = 2 with
+ * positive multiple of 16 (both 0 needs text_len > 0), frames not in
+ * {0, 1, 2}, frames = 2 with
  * rope_axes 2, rope_axes not 2 or 3, total tokens >= 2^31, short or
  * misaligned workspace), MF_ERR_UNSUPPORTED, MF_ERR_BUDGET, MF_ERR_CUDA. */
 MF_API mf_status mf_pack_plan(const mf_sample *samples, int32_t n_samples, int32_t token_budget,

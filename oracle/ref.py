@@ -71,6 +71,7 @@ TEXT_POS = -1
 def pack_plan(samples, token_budget: int = 0):
     """Plan a pack from per-sample (text_len, height_px, width_px[, frames]).
 
+    A sample with height = width = 0 and text is text-only (no image rows).
     ``frames`` (default 1) is 1 for a generation sample and 2 for an edit
     sample, whose source and target latents (same size) follow its text as
     frames 0 and 1.  The samples are taken in order; the pack is the longest
@@ -87,7 +88,8 @@ def pack_plan(samples, token_budget: int = 0):
     for smp in samples:
         t, h, w = smp[:3]
         nf = smp[3] if len(smp) > 3 else 1
-        if t < 0 or h <= 0 or w <= 0 or h % PATCH or w % PATCH or nf not in (1, 2):
+        text_only = h == 0 and w == 0 and t > 0       # a sample without an image
+        if t < 0 or (not text_only and (h <= 0 or w <= 0)) or h % PATCH or w % PATCH or nf not in (1, 2):
             raise ValueError(f"invalid sample {tuple(smp)}")
         gh, gw = h // PATCH, w // PATCH
         lens.append(t + nf * gh * gw)

@@ -60,7 +60,9 @@ mf_status check_samples(const mf_sample* samples, int32_t n, int32_t budget, int
   bool stopped = false;
   for (int32_t i = 0; i < n; ++i) {
     const mf_sample& s = samples[i];
-    if (s.text_len < 0 || s.height <= 0 || s.width <= 0 || (s.height % 16) || (s.width % 16))
+    // height = width = 0: a text-only sample (it must then have text)
+    const bool text_only = s.height == 0 && s.width == 0 && s.text_len > 0;
+    if (s.text_len < 0 || (!text_only && (s.height <= 0 || s.width <= 0)) || (s.height % 16) || (s.width % 16))
       return MF_ERR_INVALID_ARG;
     if (s.frames < 0 || s.frames > 2 || (sample_frames(s) == 2 && rope_axes != 3)) return MF_ERR_INVALID_ARG;
     const long long gh = s.height / 16, gw = s.width / 16;

@@ -48,8 +48,9 @@ def _ws_size(L, samples, budget=0, head_dim=128, rope_axes=2):
 def test_plan_validation_without_gpu(L):
     assert _ws_size(L, [(17, 128, 128), (9, 64, 256)])[0] == 0
     assert _ws_size(L, [])[0] == 0
-    for bad in [(-1, 16, 16), (0, 0, 16), (0, 16, 24), (3, 17, 16), (0, -16, 16)]:
+    for bad in [(-1, 16, 16), (0, 0, 16), (0, 16, 24), (3, 17, 16), (0, -16, 16), (0, 0, 0)]:
         assert _ws_size(L, [bad])[0] == 1, bad
+    assert _ws_size(L, [(7, 0, 0), (0, 16, 16)])[0] == 0   # text-only sample
     assert _ws_size(L, [(0, 16, 16)], head_dim=96)[0] == 2
     assert _ws_size(L, [(0, 16 * 1025, 16)])[0] == 2
     assert _ws_size(L, [(100, 64, 64)], budget=50)[0] == 3

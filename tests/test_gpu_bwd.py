@@ -57,6 +57,12 @@ def test_bwd_tile_boundaries(L):
     _run_full([(0, 16, 16 * L)], heads=2, head_dim=128, seed=L)
 
 
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_bwd_text_only_and_image_only_samples(head_dim):
+    _run_full([(40, 0, 0), (0, 48, 48), (1, 0, 0), (129, 0, 0), (3, 32, 32), (0, 16, 16 * 127)],
+              heads=2, head_dim=head_dim, seed=head_dim)
+
+
 def test_bwd_single_token_closed_form():
     """One key: P = 1, dS = 0, so dQ = dK = 0 and dV = dO."""
     plan, (q, k, v, do), (dq, dk, dv) = _gpu_fwd_bwd([(0, 16, 16), (1, 16, 16)], 2, 128, 3)

@@ -49,6 +49,14 @@ def test_fwd_tile_boundaries(L):
     _run_full([(0, 16, 16 * L)], heads=2, head_dim=128, seed=L)
 
 
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_fwd_text_only_and_image_only_samples(head_dim):
+    # text-only samples (no image: unrotated), image-only samples, a 1-token
+    # text-only sample, lengths around the tile edges
+    _run_full([(40, 0, 0), (0, 48, 48), (1, 0, 0), (129, 0, 0), (3, 32, 32), (0, 16, 16 * 127)],
+              heads=2, head_dim=head_dim, seed=head_dim)
+
+
 def test_fwd_custom_scale_and_budget():
     samples = [(30, 96, 96), (12, 64, 48), (0, 48, 160)]
     _run_full(samples, heads=2, head_dim=64, seed=4, scale=0.3)

@@ -72,6 +72,11 @@ def test_plan_edit_packs(seed, head_dim):
     _check_plan(synth.random_pack(200 + seed, 5, 40, 12), 0, head_dim, rope_axes=3)
 
 
+def test_plan_text_only_samples():
+    _check_plan([(40, 0, 0), (3, 32, 32), (1, 0, 0), (0, 16, 16)], 0)
+    _check_plan([(5, 0, 0), (2, 32, 16, 2)], 0, rope_axes=3)
+
+
 def test_plan_edit_needs_three_axes():
     with pytest.raises(mf.MfError) as ei:
         mf.pack_plan([(4, 32, 32, 2)], rope_axes=2)

@@ -105,9 +105,13 @@ def test_pack_plan_budget_prefix():
     assert oracle.pack_plan(samples, 0)["n_samples"] == 3
     with pytest.raises(ValueError):
         oracle.pack_plan(samples, 25)
-    for bad in [(-1, 16, 16), (0, 0, 16), (0, 16, 24), (3, 17, 16)]:
+    for bad in [(-1, 16, 16), (0, 0, 16), (0, 16, 24), (3, 17, 16), (0, 0, 0)]:
         with pytest.raises(ValueError):
             oracle.pack_plan([bad], 0)
+    # a text-only sample (no image): all of its rows are text, none rotated
+    p = oracle.pack_plan([(4, 0, 0), (1, 16, 16)])
+    assert list(p["cu_seqlens"]) == [0, 4, 6] and p["max_grid"] == 1
+    assert [tuple(r) for r in p["pos"]] == [(-1, -1)] * 5 + [(0, 0)]
     empty = oracle.pack_plan([], 0)
     assert empty["total_tokens"] == 0 and list(empty["cu_seqlens"]) == [0]
 
