@@ -28,8 +28,8 @@
  *     16-byte aligned.  LSE is float32 [heads, total_tokens], natural log of
  *     the scaled logits' sum of exponentials.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
- *     launch is enqueued on it.  Only mf_pack_plan and mf_check synchronize
- *     it (to return scalars); the attention calls never do.
+ *     launch is enqueued on it.  Only mf_check synchronizes it (to read the
+ *     status word); mf_pack_plan and the attention calls never do.
  *   - The library allocates no device memory: the caller passes workspaces
  *     sized by the *_workspace_size calls.  It keeps no state besides a
  *     per-thread copy of the last CUDA error message.
@@ -139,8 +139,14 @@ MF_API mf_status mf_pack_plan_workspace_size(const mf_sample *samples, int32_t n
  *   workspace    device memory of at least mf_pack_plan_workspace_size bytes,
  *                256-byte aligned
  *   plan_out     host struct, filled on success
- * Runs a device prefix scan, the per-token id expansion and the RoPE table on
- * `stream`, then synchronizes `stream` once to read the scalars back.
+ * The host computes the plan's scalars (packed count, total tokens, maxima,
+ * tile and tile-pair counts) from `samples` and returns without waiting on
+ * `stream`; the device prefix scan, the per-token id expansion and the RoPE
+ * table run on `stream`.  The scan recomputes the scalars and, if they differ
+ * from the host's, sets the status word so that mf_check fails with
+ * MF_ERR_CUDA.  `samples` is copied with cudaMemcpyAsync: pageable memory is
+ * free for reuse on return, page-locked memory only once `stream` has run
+ * the copy.
  * Errors: MF_ERR_INVALID_ARG (null pointer, text_len < 0, H or W not a
  * positive multiple of 16 (both 0 needs text_len > 0), frames not in
  * {0, 1, 2}, frames = 2 with
@@ -279,8 +285,9 @@ MF_API mf_status mf_cfg_combine(const void *o, const mf_plan *plan, int32_t head
                                 float guidance, void *out, void *stream);
 
 /* Synchronize `stream`, then read and clear the plan's device status word:
- * MF_OK, MF_ERR_TIMEOUT, MF_ERR_RANGE, or MF_ERR_CUDA for a failed
- * synchronization. */
+ * MF_OK, MF_ERR_TIMEOUT, MF_ERR_RANGE, MF_ERR_INVALID_ARG (a mismatched CFG
+ * pair), or MF_ERR_CUDA for a failed synchronization, a misaligned shared-
+ * memory window or a device pack scan that disagreed with the host's plan. */
 MF_API mf_status mf_check(const mf_plan *plan, void *stream);
 
 /* Profiling aid: the next mf_attn_fwd or mf_attn_bwd call made by this

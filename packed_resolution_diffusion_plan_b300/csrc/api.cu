@@ -44,6 +44,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct PlanLayout {
   size_t off_scalars, off_samples, off_cu, off_order, off_pos, off_frame, off_rope, off_rope_f, bytes;
   int32_t token_bound, grid_bound;
+  mf::PlanScalars expect;  // the plan's scalars, from the same greedy prefix rule as the device scan
 };
 
 // Latent frames of a sample (0 counts as 1).
@@ -55,8 +56,8 @@ mf_status check_samples(const mf_sample* samples, int32_t n, int32_t budget, int
   if (rope_axes != 2 && rope_axes != 3) return MF_ERR_INVALID_ARG;
   if (n > MF_MAX_SAMPLES) return MF_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
-  long long used = 0;
-  int32_t gmax = 0;
+  long long used = 0, n_tiles = 0, n_pairs = 0;
+  int32_t gmax = 0, n_packed = 0, max_len = 0, max_grid = 0;
   bool stopped = false;
   for (int32_t i = 0; i < n; ++i) {
     const mf_sample& s = samples[i];
@@ -76,9 +77,21 @@ mf_status check_samples(const mf_sample* samples, int32_t n, int32_t budget, int
       } else {
         used += len;
         if (used >= (1ll << 31)) return MF_ERR_INVALID_ARG;
+        ++n_packed;
+        max_len = static_cast<int32_t>(std::max<long long>(max_len, len));
+        max_grid = static_cast<int32_t>(std::max<long long>(max_grid, std::max(gh, gw)));
+        n_tiles += (len + mf::kTile - 1) / mf::kTile;
+        n_pairs += (len + 2 * mf::kTile - 1) / (2 * mf::kTile);
       }
     }
   }
+  L->expect = mf::PlanScalars{};
+  L->expect.n_packed = n_packed;
+  L->expect.total_tokens = static_cast<int32_t>(used);
+  L->expect.max_seqlen = max_len;
+  L->expect.max_grid = max_grid;
+  L->expect.n_tiles = static_cast<int32_t>(n_tiles);
+  L->expect.n_pairs = static_cast<int32_t>(n_pairs);
   L->token_bound = static_cast<int32_t>(used);
   L->grid_bound = gmax;
   size_t off = 0;
@@ -258,6 +271,7 @@ mf_status mf_pack_plan(const mf_sample* samples, int32_t n_samples, int32_t toke
   a.head_dim = head_dim;
   a.rope_axes = rope_axes;
   a.theta = rope_theta;
+  a.expect = L.expect;
   cudaError_t e;
   if (n_samples > 0) {
     e = cudaMemcpyAsync(ws + L.off_samples, samples, static_cast<size_t>(n_samples) * sizeof(mf_sample),
@@ -266,18 +280,16 @@ mf_status mf_pack_plan(const mf_sample* samples, int32_t n_samples, int32_t toke
   }
   e = mf::launch_pack_plan(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "mf_pack_plan: launch");
-  PlanScalars sc;
-  e = cudaMemcpyAsync(&sc, ws + L.off_scalars, sizeof(sc), cudaMemcpyDeviceToHost, s);
-  if (e != cudaSuccess) return cuda_fail(e, "mf_pack_plan: read scalars");
-  e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return cuda_fail(e, "mf_pack_plan: synchronize");
-  plan_out->n_samples = sc.n_packed;
-  plan_out->total_tokens = sc.total_tokens;
-  plan_out->max_seqlen = sc.max_seqlen;
-  plan_out->max_grid = sc.max_grid;
+  // The scalars come from the host pass above, so the call never waits on
+  // `stream`; the device scan recomputes them and raises kStatusPlan if it
+  // disagrees.
+  plan_out->n_samples = L.expect.n_packed;
+  plan_out->total_tokens = L.expect.total_tokens;
+  plan_out->max_seqlen = L.expect.max_seqlen;
+  plan_out->max_grid = L.expect.max_grid;
   plan_out->head_dim = head_dim;
-  plan_out->n_tiles = sc.n_tiles;
-  plan_out->n_pairs = sc.n_pairs;
+  plan_out->n_tiles = L.expect.n_tiles;
+  plan_out->n_pairs = L.expect.n_pairs;
   plan_out->cu_seqlens = a.cu_seqlens;
   plan_out->pos = a.pos;
   plan_out->frame = a.frame;
@@ -439,6 +451,10 @@ mf_status mf_check(const mf_plan* plan, void* stream) {
     e = cudaMemsetAsync(plan->status, 0, sizeof(int32_t), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "mf_check: clear status");
+    if (status & mf::kStatusPlan) {
+      g_last_cuda_error = "the device pack scan disagreed with the host's plan scalars";
+      return MF_ERR_CUDA;
+    }
     if (status & mf::kStatusLayout) {
       g_last_cuda_error = "a kernel found its shared memory misaligned and did no work";
       return MF_ERR_CUDA;

@@ -40,6 +40,7 @@ struct PlanArgs {
   int32_t head_dim;
   int32_t rope_axes;        // 2 or 3
   float theta;
+  PlanScalars expect;       // the host's scalars for this pack (the scan checks its own against them)
 };
 
 cudaError_t launch_pack_plan(const PlanArgs& a, cudaStream_t stream);

@@ -6,6 +6,7 @@
 // fixed token budget and attention is confined by per-sample cumulative
 // offsets; section "Mage-VAE": an H x W px image becomes (H/16)(W/16) tokens.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace mf {
 namespace {
@@ -138,7 +139,10 @@ __global__ void __launch_bounds__(kPlanThreads) pack_scan_kernel(PlanArgs a) {
     a.scalars->max_grid = s_maxgrid;
     a.scalars->n_tiles = static_cast<int32_t>(n_tiles);
     a.scalars->n_pairs = static_cast<int32_t>(n_pairs);
-    a.scalars->status = 0;
+    const PlanScalars& x = a.expect;
+    const bool same = x.n_packed == np && x.total_tokens == total && x.max_seqlen == s_maxlen &&
+                      x.max_grid == s_maxgrid && x.n_tiles == n_tiles && x.n_pairs == n_pairs;
+    a.scalars->status = same ? 0 : kStatusPlan;
   }
 }
 

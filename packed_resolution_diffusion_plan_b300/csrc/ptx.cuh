@@ -29,6 +29,9 @@ constexpr int kStatusLayout = 4;
 // A classifier-free-guidance pair whose two samples have different image
 // sizes (mf_cfg_combine skipped its rows).
 constexpr int kStatusPairing = 8;
+// The device pack scan's scalars differ from those the host returned in the
+// plan (the host and device packing rules disagree).
+constexpr int kStatusPlan = 16;
 // Largest finite fp16 magnitude: the logit MMA's operands must stay below it.
 constexpr float kF16Max = 65504.0f;
 

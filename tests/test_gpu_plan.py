@@ -17,7 +17,10 @@ def _check_plan(samples, budget, head_dim=128, theta=10000.0, rope_axes=2):
     ref = oracle.pack_plan(samples, budget)
     p = mf.pack_plan(samples, token_budget=budget, head_dim=head_dim, rope_theta=theta, rope_axes=rope_axes)
     assert p.rope_axes == rope_axes
-    mf.check(p)
+    mf.check(p)   # also fails if the device scan's scalars differ from the host's
+    # the scan's own scalars (the workspace's first 32 bytes) are the plan's
+    got = p.workspace[:32].view(torch.int32).cpu().tolist()
+    assert got[:5] + got[6:7] == [p.n_samples, p.total_tokens, p.max_seqlen, p.max_grid, p.n_tiles, p.n_pairs]
     assert p.n_samples == ref["n_samples"]
     assert p.total_tokens == ref["total_tokens"]
     assert p.max_seqlen == ref["max_seqlen"]
