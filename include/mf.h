@@ -201,6 +201,33 @@ MF_API mf_status mf_attn_bwd(const void *q, const void *k, const void *v, const 
                       int32_t head_dim, float softmax_scale, void *workspace,
                       size_t workspace_bytes, void *dq, void *dk, void *dv, void *stream);
 
+/* Bytes of device workspace mf_attn_bwd_rotated needs: the float32 row dots
+ * D and the float32 dQ accumulator (the rotated copies are the forward's). */
+MF_API mf_status mf_attn_bwd_rotated_workspace_size(int32_t total_tokens, int32_t heads,
+                                                    int32_t head_dim, size_t *bytes);
+
+/* mf_attn_bwd from the rotated Q and K that the forward left in its own
+ * workspace (mf_attn_fwd or mf_attn_fwd_qkv with the same plan, heads,
+ * head_dim and softmax_scale): a training step keeps that workspace from the
+ * forward to the backward in place of Q and K.  The gradients are the same
+ * as mf_attn_bwd's (review, section "Native-Resolution MMDiT"; dQ and dK are
+ * taken with respect to the unrotated inputs), but the backward skips
+ * rotating Q and K again and recomputes exactly the forward's fp16 logit
+ * operands.
+ *   fwd_workspace        device; the forward's workspace, unchanged since that
+ *                        call (fp16 q~ = s log2(e) R(q), then k~ = R(k));
+ *                        256-byte aligned, >= mf_attn_fwd_workspace_size bytes
+ *   workspace            device, >= mf_attn_bwd_rotated_workspace_size bytes,
+ *                        256-byte aligned
+ *   softmax_scale        the forward's (<= 0 selects 1/sqrt(head_dim) in both)
+ * Other arguments, results and errors as mf_attn_bwd (no Q or K arguments). */
+MF_API mf_status mf_attn_bwd_rotated(const void *fwd_workspace, size_t fwd_workspace_bytes,
+                                     const void *v, const void *o, const float *lse,
+                                     const void *dout, const mf_plan *plan, int32_t heads,
+                                     int32_t head_dim, float softmax_scale, void *workspace,
+                                     size_t workspace_bytes, void *dq, void *dk, void *dv,
+                                     void *stream);
+
 /* Size of the fixed device scratch behind mf_attn_bwd_noalloc (128 MiB). */
 #define MF_NOALLOC_SCRATCH_BYTES (128u * 1024u * 1024u)
 

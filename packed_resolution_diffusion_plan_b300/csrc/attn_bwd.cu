@@ -54,7 +54,6 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kReduceWarp = 10;
 constexpr int kRowWarp = 11;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 // Per-thread register shares after setmaxnreg; they add up to the launch's
 // 3 x 168 per thread (65,536 / 384 rounded down to a multiple of 8).
@@ -97,11 +96,12 @@ struct BwdCfg {
 
 // ---------------------------------------------------------------- bwd_pre
 // One thread per (token, head, 8-column chunk); a group of D/8 lanes reduces
-// one row of D.  The thread also zeroes the matching 8 accumulator floats and
-// writes the chunk of q~ = R(q) and of k~ = s log2(e) R(k) as fp16: the main
-// kernel streams every Q tile once per K/V tile of its sample, so rotating
-// here, once per token, replaces that many rotations of each tile.  A value
-// beyond the fp16 range (or a NaN) raises the range status.
+// one row of D.  The thread also zeroes the matching 8 accumulator floats and,
+// unless the backward reads the forward's rotated copies, writes the chunk of
+// q~ = R(q) and of k~ = s log2(e) R(k) as fp16: the main kernel streams every
+// Q tile once per K/V tile of its sample, so rotating here, once per token,
+// replaces that many rotations of each tile.  A value beyond the fp16 range
+// (or a NaN) raises the range status.
 template <int D>
 __global__ void bwd_pre_kernel(const BwdArgs a) {
   constexpr int kChunks = D / 8;
@@ -114,18 +114,21 @@ __global__ void bwd_pre_kernel(const BwdArgs a) {
     const long long tok = row / a.g.heads;
     const uint4 o = reinterpret_cast<const uint4*>(a.o)[gid];
     const uint4 g = reinterpret_cast<const uint4*>(a.dout)[gid];
-    const uint4 qv = reinterpret_cast<const uint4*>(a.q)[gid];
-    const uint4 kv = reinterpret_cast<const uint4*>(a.k)[gid];
     const uint32_t* ow = reinterpret_cast<const uint32_t*>(&o);
     const uint32_t* gw = reinterpret_cast<const uint32_t*>(&g);
-    const uint32_t* qw = reinterpret_cast<const uint32_t*>(&qv);
-    const uint32_t* kw = reinterpret_cast<const uint32_t*>(&kv);
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       acc += bf16_lo(ow[e]) * bf16_lo(gw[e]) + bf16_hi(ow[e]) * bf16_hi(gw[e]);
     float4* z = reinterpret_cast<float4*>(a.dq_acc) + gid * 2;
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (row < rows && a.rotate) {
+    const long long tok = row / a.g.heads;
+    const uint4 qv = reinterpret_cast<const uint4*>(a.q)[gid];
+    const uint4 kv = reinterpret_cast<const uint4*>(a.k)[gid];
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(&qv);
+    const uint32_t* kw = reinterpret_cast<const uint32_t*>(&kv);
     // the chunk's four rotation pairs (rope_pair_cs; text is not rotated)
     const int2 p = reinterpret_cast<const int2*>(a.g.pos)[tok];
     const int fr = a.g.frame[tok];
@@ -157,9 +160,9 @@ __global__ void bwd_pre_kernel(const BwdArgs a) {
 }
 
 // ---------------------------------------------------------------- bwd_dq
-// dq = R^T (ln 2 * acc): the accumulator holds dS k~ with k~ pre-scaled by
-// s * log2 e, so s dS k~ = ln 2 * acc.  One thread per (token, head,
-// 8-column chunk).
+// dq = R^T (dq_mult * acc): the accumulator holds dS k~, so s dS R(k) is
+// ln 2 * acc when k~ carries the s log2(e) factor and s * acc when q~ does.
+// One thread per (token, head, 8-column chunk).
 template <int D>
 __global__ void bwd_dq_kernel(const BwdArgs a) {
   constexpr int kChunks = D / 8;
@@ -197,12 +200,12 @@ __global__ void bwd_dq_kernel(const BwdArgs a) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float c = cs[2 * e], s = cs[2 * e + 1];
-      const float u0 = x[2 * e] * kLn2, u1 = x[2 * e + 1] * kLn2;
+      const float u0 = x[2 * e] * a.dq_mult, u1 = x[2 * e + 1] * a.dq_mult;
       out[e] = pack_bf16(fmaf(u0, c, u1 * s), fmaf(-u0, s, u1 * c));
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) out[e] = pack_bf16(x[2 * e] * kLn2, x[2 * e + 1] * kLn2);
+    for (int e = 0; e < 4; ++e) out[e] = pack_bf16(x[2 * e] * a.dq_mult, x[2 * e + 1] * a.dq_mult);
   }
   reinterpret_cast<uint4*>(a.dq)[gid] = make_uint4(out[0], out[1], out[2], out[3]);
 }
@@ -661,9 +664,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         uint32_t v[32];
         tmem_ld32(tl + C::kColDK + col0, v);
         tmem_wait_ld(v);
-        // TMEM holds dS^T q~; dk~ = s dS^T q~.
+        // TMEM holds dS^T q~; dk~ = dk_mult dS^T q~ (s, or ln 2 when q~ carries s log2 e).
         if (kv_valid)
-          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dk) + rowoff, v, col0, args.scale, pk, fk,
+          store_row_chunk<D>(reinterpret_cast<__nv_bfloat16*>(args.dk) + rowoff, v, col0, args.dk_mult, pk, fk,
                              args.g, true);
       }
     }

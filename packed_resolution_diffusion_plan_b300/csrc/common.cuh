@@ -109,8 +109,14 @@ struct BwdArgs {
   const void* dout;
   const float* lse;
   float* dsum;               // [heads, T] rowsum(dO * O)
-  void* q_rot;               // fp16 [T, heads, D] q~ = R(q)
-  void* k_rot;               // fp16 [T, heads, D] k~ = s log2(e) R(k)
+  // fp16 [T, heads, D] rotated copies, one of them scaled by s log2(e):
+  // written by bwd_pre (q~ = R(q), k~ = s log2(e) R(k)) when rotate is set,
+  // else the forward's own (q~ = s log2(e) R(q), k~ = R(k)).
+  void* q_rot;
+  void* k_rot;
+  int rotate;
+  float dk_mult;             // dk~ = dk_mult * (dS^T q~): s, or ln 2 with the forward's copies
+  float dq_mult;             // dq~ = dq_mult * (dS k~): ln 2, or s with the forward's copies
   float* dq_acc;             // [T, heads, D] float32 accumulator (zeroed by the preprocess)
   void* dq;
   void* dk;

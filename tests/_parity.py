@@ -22,9 +22,10 @@ def rel_l2(a, b):
 
 
 def lse_tol_factor(scale, head_dim):
-    """The LSE bound is stated for the default scale 1/sqrt(d).  The logit
-    rounding error is proportional to the logits' size, s * |q~||k~| ~ s*sqrt(d),
-    so a non-default scale widens the bound by s * sqrt(d) (never tightens it)."""
+    """The LSE and gradient bounds are stated for the default scale 1/sqrt(d).
+    The logit rounding error is proportional to the logits' size,
+    s * |q~||k~| ~ s*sqrt(d), and dQ, dK carry the factor s themselves, so a
+    non-default scale widens the bounds by s * sqrt(d) (never tightens them)."""
     if not scale or scale <= 0:
         return 1.0
     return max(1.0, scale * np.sqrt(head_dim))

@@ -72,6 +72,33 @@ def test_attn_fwd_qkv_equals_split_tensors(head_dim, heads):
 
 
 @pytest.mark.parametrize("rope_axes", [2, 3])
+def test_bwd_rotated_from_qkv_forward(rope_axes):
+    """The backward from the rotated copies that the QKV-row forward leaves in
+    its workspace, against the oracle's gradients."""
+    heads, head_dim = 4, 128
+    samples = synth.random_pack(700 + rope_axes, 4, 70, 12, edit=rope_axes == 3)
+    plan = mf.pack_plan(samples, head_dim=head_dim, rope_axes=rope_axes)
+    g = torch.Generator("cpu").manual_seed(rope_axes)
+    T, C = plan.total_tokens, heads * head_dim
+    qkv = _bf16(g, T, 3 * C)
+    do = _bf16(g, T, heads, head_dim)
+    wsf = torch.empty(max(256, mf.fwd_workspace_bytes(T, heads, head_dim)), dtype=torch.uint8, device="cuda")
+    o, lse = mf.attn_fwd_qkv(qkv, plan, heads, workspace=wsf)
+    v = qkv[:, 2 * C:].contiguous().view(T, heads, head_dim)
+    dq, dk, dv = mf.attn_bwd_rotated(wsf, v, o, lse, do, plan)
+    mf.check(plan)
+    q, k = (qkv[:, i * C:(i + 1) * C].contiguous().view(T, heads, head_dim) for i in range(2))
+    ref = oracle.pack_plan(samples)
+    rope = dict(frame=ref["frame"], rope_axes=rope_axes)
+    qn, kn, vn = to64(q), to64(k), to64(v)
+    O, L = oracle.attn_fwd(qn, kn, vn, ref["cu_seqlens"], ref["pos"], **rope)
+    rq, rk, rv = oracle.attn_bwd(qn, kn, vn, O, L, to64(do), ref["cu_seqlens"], ref["pos"], **rope)
+    assert_close("dV", to64(dv), rv, "grad")
+    assert_close("dK", to64(dk), rk, "grad")
+    assert_close("dQ", to64(dq), rq, "grad")
+
+
+@pytest.mark.parametrize("rope_axes", [2, 3])
 def test_attention_block_end_to_end(rope_axes):
     """x -> norm_modulate -> @W_qkv -> attn_fwd_qkv -> @W_o -> gate_residual
     against the oracle's float64 block (bf16 intermediates on the GPU: the

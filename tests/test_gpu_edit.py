@@ -23,7 +23,9 @@ def _run(samples, heads, head_dim, seed, bwd=True):
     t = synth.draw_tensors(wl, with_grad=bwd)
     plan = mf.pack_plan(samples, head_dim=head_dim, rope_axes=3)
     q, k, v = (t[n].cuda() for n in ("q", "k", "v"))
-    o, lse = mf.attn_fwd(q, k, v, plan)
+    wsf = torch.empty(max(256, mf.fwd_workspace_bytes(plan.total_tokens, heads, head_dim)), dtype=torch.uint8,
+                      device="cuda")
+    o, lse = mf.attn_fwd(q, k, v, plan, workspace=wsf)
     mf.check(plan)
     ref = oracle.pack_plan(samples)
     rope = dict(frame=ref["frame"], rope_axes=3)
@@ -34,12 +36,13 @@ def _run(samples, heads, head_dim, seed, bwd=True):
     if not bwd:
         return
     do = t["do"].cuda()
-    dq, dk, dv = mf.attn_bwd(q, k, v, o, lse, do, plan)
-    mf.check(plan)
     rq, rk, rv = oracle.attn_bwd(qn, kn, vn, O, L, to64(do), ref["cu_seqlens"], ref["pos"], **rope)
-    assert_close("dV", to64(dv), rv, "grad")
-    assert_close("dK", to64(dk), rk, "grad")
-    assert_close("dQ", to64(dq), rq, "grad")
+    # both backward entry points: Q and K rotated again, or the forward's copies
+    for dq, dk, dv in (mf.attn_bwd(q, k, v, o, lse, do, plan), mf.attn_bwd_rotated(wsf, v, o, lse, do, plan)):
+        mf.check(plan)
+        assert_close("dV", to64(dv), rv, "grad")
+        assert_close("dK", to64(dk), rk, "grad")
+        assert_close("dQ", to64(dq), rq, "grad")
 
 
 @pytest.mark.parametrize("head_dim", [64, 128])
