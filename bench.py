@@ -57,6 +57,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-threads", type=int, default=0, help="BLAS threads of the oracle baseline (0: all)")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--bwd", choices=["rotated", "plain"], default="rotated",
                     help="backward entry: from the forward's rotated copies, or from Q and K")
@@ -150,18 +151,36 @@ class ClockSampler:
 # oracle (CPU) baseline
 # --------------------------------------------------------------------------
 
+_BLAS_ENV = ("OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "OMP_NUM_THREADS")
+
+
 def _blas_threads():
     try:
         import threadpoolctl
         info = threadpoolctl.threadpool_info()
         return int(max(i.get("num_threads", 1) for i in info)) if info else 1
     except Exception:
+        for var in _BLAS_ENV:
+            if os.environ.get(var, "").isdigit():
+                return int(os.environ[var])
         return os.cpu_count() or 1
 
 
-def oracle_sample(wl, seconds, max_heads=None):
+def oracle_sample(wl, seconds, max_heads=None, threads=0):
     """Time the oracle's fwd+bwd on one sample of the workload, head after
-    head, until `seconds` of CPU work (or all heads) are done."""
+    head, until `seconds` of CPU work (or all heads) are done; `threads` > 0
+    caps the BLAS threads (0: all of them)."""
+    if threads > 0:
+        try:
+            import threadpoolctl
+        except ImportError:
+            # without threadpoolctl the BLAS pool is sized at start-up only
+            if _blas_threads() != threads:
+                raise SystemExit(f"--cpu-threads {threads}: start with " +
+                                 " ".join(f"{v}={threads}" for v in _BLAS_ENV) + " (threadpoolctl is missing)")
+            return oracle_sample(wl, seconds, max_heads)
+        with threadpoolctl.threadpool_limits(limits=threads):
+            return oracle_sample(wl, seconds, max_heads)
     import oracle
     lens = [sample_len(s) for s in wl.samples]
     # the sample whose length is closest to 3,600 tokens: large enough to be
@@ -298,9 +317,11 @@ def run_mf(args):
         backward(q, k, v, o, lse, do, plan, ws, ws_fwd, dq, dk, dv)
         return plan
 
+    # Each step plans anew, and every plan carries its own status word: check
+    # them all, so that a timeout in any step fails the run.
     for _ in range(max(args.warmup, 1)):
         plan = step()
-    mf.check(plan)
+        mf.check(plan)
     launches_per_step = 3 + 2 + 3  # scan, ids, RoPE table; fwd pre, main; bwd pre, main, dq
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
@@ -311,14 +332,14 @@ def run_mf(args):
     torch.cuda.synchronize(dev)
     clocks.start()
     t_start.record(stream)
-    for i in range(args.steps):
-        plan = step(evs[i])
+    plans = [step(evs[i]) for i in range(args.steps)]
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    mf.check(plan)
+    for plan in plans:
+        mf.check(plan)
     ms_step = t_start.elapsed_time(t_end) / args.steps
     fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     bwd_main_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
@@ -411,7 +432,7 @@ def run_mf(args):
                 "per_kernel": {n: {k2: round(v2, 4) for k2, v2 in kd.items()} for n, kd in kernels.items()}}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_sample(wl, args.cpu_seconds)
+        cpu = oracle_sample(wl, args.cpu_seconds, threads=args.cpu_threads)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

@@ -37,7 +37,10 @@
  *     returns MF_ERR_INVALID_ARG and leaves every buffer untouched.
  *   - Every wait inside a kernel is bounded (a few seconds).  A kernel that
  *     gives up sets the plan's device status word and exits cleanly;
- *     mf_check() reports it as MF_ERR_TIMEOUT.
+ *     mf_check() reports it as MF_ERR_TIMEOUT, and mf_last_cuda_error() then
+ *     names the kernel, the barrier of the first timeout and how many CTAs
+ *     gave up.  Every plan carries its own status: check each plan whose
+ *     kernels ran.
  *   - softmax_scale <= 0 selects 1/sqrt(head_dim).
  *   - Precision: Q, K, V, O and the gradients are bf16 with fp32
  *     accumulation.  The logit product R(Q) R(K)^T is computed from fp16
@@ -343,7 +346,8 @@ MF_API mf_status mf_debug_inject(int32_t flags);
 /* Static description of a status code. */
 MF_API const char *mf_status_string(mf_status status);
 
-/* Message of the last CUDA error seen by this thread ("" if none). */
+/* Message of the last CUDA error seen by this thread, or of the last timeout
+ * mf_check reported ("" if none). */
 MF_API const char *mf_last_cuda_error(void);
 
 #ifdef __cplusplus

@@ -110,7 +110,7 @@ def lib():
 
 def _raise(status: int, where: str):
     if status != 0:
-        detail = lib().mf_last_cuda_error().decode() if status == 4 else ""
+        detail = lib().mf_last_cuda_error().decode() if status in (4, 5) else ""
         raise MfError(status, where, detail)
 
 

@@ -2,6 +2,7 @@
 // workspace layout, TMA descriptor encoding and kernel launches.  No device
 // memory is allocated here; every buffer comes from the caller.
 #include <cmath>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -219,6 +220,10 @@ mf::AttnGeom make_geom(const mf_plan* plan, int32_t heads) {
   g.heads = heads;
   g.n_items = plan->n_tiles * heads;
   g.status = plan->status;
+  // the timeout record sits two words after the status word (PlanScalars)
+  static_assert(offsetof(mf::PlanScalars, timeout_info) - offsetof(mf::PlanScalars, status) == 2 * sizeof(int32_t),
+                "timeout record beside the status word");
+  g.timeout_info = plan->status + 2;
   g.debug = g_debug_flags;
   return g;
 }
@@ -515,14 +520,25 @@ mf_status mf_check(const mf_plan* plan, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "mf_check: synchronize");
-  int32_t status = 0;
-  e = cudaMemcpyAsync(&status, plan->status, sizeof(status), cudaMemcpyDeviceToHost, s);
+  // status, n_pairs, timeout record (PlanScalars from the status word on)
+  int32_t words[3] = {0, 0, 0};
+  e = cudaMemcpyAsync(words, plan->status, sizeof(words), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "mf_check: read status");
+  const int32_t status = words[0];
   if (status != 0) {
     e = cudaMemsetAsync(plan->status, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(plan->status + 2, 0, sizeof(int32_t), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "mf_check: clear status");
+    if (status & mf::kStatusTimeout) {
+      const uint32_t info = static_cast<uint32_t>(words[2]);
+      char buf[160];
+      snprintf(buf, sizeof(buf), "a bounded wait timed out in %s: first at barrier %u, %u CTA(s)",
+               (info >> 28) == 1 ? "attn_fwd_kernel" : (info >> 28) == 2 ? "bwd_main_kernel" : "a kernel",
+               (info >> 16) & 0xfffu, info & 0xffffu);
+      g_last_cuda_error = buf;
+    }
     if (status & mf::kStatusPlan) {
       g_last_cuda_error = "the device pack scan disagreed with the host's plan scalars";
       return MF_ERR_CUDA;

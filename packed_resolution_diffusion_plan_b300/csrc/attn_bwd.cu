@@ -63,6 +63,12 @@ static_assert(2 * kRegsCompute + kRegsCtrl <= 3 * 168, "warpgroup register share
 // Barriers and CTA-wide scalars of bwd_main, kept in dynamic shared memory
 // after the tiles (the kernel has no static shared memory, so the dynamic
 // base is the start of the CTA's window and the tiles stay 1024-aligned).
+// A timeout record names a barrier by its position here: kv_full 0, fin 1,
+// q_full 2-3, q_ready 4-5, q_free 6-7, do_full 8, do_free 9, s_full 10,
+// p_ready 11, dp_full 12, ds_ready 13, a_free 14, dq_full 15, dq_free 16,
+// stage_full 17-18, stage_free 19, q_issued 20.
+constexpr uint32_t kBwdBarriers = 21;
+constexpr uint32_t kTimeoutKernelBwd = 2;
 struct BwdCtl {
   uint64_t kv_full, fin;
   uint64_t q_full[2], q_ready[2], q_free[2], do_full, do_free;
@@ -111,7 +117,6 @@ __global__ void bwd_pre_kernel(const BwdArgs a) {
   const int ch = static_cast<int>(gid % kChunks);
   float acc = 0.f;
   if (row < rows) {
-    const long long tok = row / a.g.heads;
     const uint4 o = reinterpret_cast<const uint4*>(a.o)[gid];
     const uint4 g = reinterpret_cast<const uint4*>(a.dout)[gid];
     const uint32_t* ow = reinterpret_cast<const uint32_t*>(&o);
@@ -278,7 +283,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       mbar_init(&c.q_full[s], 1);
       mbar_init(&c.q_ready[s], 32);  // the row warp's lanes
       // head_dim 128: dK_i has read the slot, and the reducer has read the
-      // dQ_i half staged in it
+      // dQ_i half staged in it (the producer, the row warp and warpgroup 1's
+      // next staging wait on it)
       mbar_init(&c.q_free[s], D == 128 ? 2 : 1);
       mbar_init(&c.stage_full[s], kTile);
     }
@@ -541,7 +547,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     };
     auto dq_stage = [&](int i) -> bool {
       if (D != 128) return true;
+      // Neither half may run two phases ahead of the reducer's wait on its
+      // stage_full barrier (a parity wait would then take the later phase for
+      // the one it wants and never return).  Warpgroup 0 reuses the staging
+      // tile only once the reducer has released it; warpgroup 1 stages tile i
+      // only once the reducer has taken tile i - 1's half, i.e. after the
+      // reducer's arrival on that slot's q_free (dK_{i-1} arrived long ago).
       if (cw == 0 && i >= 1 && !warp_wait(&c.stage_free, (i - 1) & 1, abort_flag)) return false;
+      if (cw == 1 && i >= 1 && !warp_wait(&c.q_free[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) return false;
       float* st = reinterpret_cast<float*>(smem + (cw == 0 ? C::kOffStage : C::kOffQ + (i & 1) * C::kTileBytes)) + r;
 #pragma unroll
       for (int j = 0; j < 64; ++j) st[j * D] = dqv[j];
@@ -679,7 +692,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (tid == 0 && c.abort) atomicOr(args.g.status, kStatusTimeout);
+  if (tid == 0 && c.abort) {
+    const uint32_t a = static_cast<uint32_t>(c.abort) - 1u, base = smem_u32(&c);
+    record_timeout(args.g.status, args.g.timeout_info, kTimeoutKernelBwd,
+                   a >= base && a < base + 8 * kBwdBarriers ? (a - base) / 8 : 0xfffu);
+  }
 }
 
 template <int D>

@@ -60,6 +60,7 @@ constexpr int kThreads = 12 * 32;
 constexpr int kCtrlWG = 2;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr uint32_t kTimeoutKernelFwd = 1;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 // Per-thread register shares after setmaxnreg; they add up to the launch's
@@ -113,10 +114,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_q_full, bar_final;
-  __shared__ uint64_t bar_k_full[C::kKStages], bar_k_free[C::kKStages];
-  __shared__ uint64_t bar_v_full[C::kVStages], bar_v_free[C::kVStages];
-  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2];
+  // One block of barriers, so that a timeout record can name one by its
+  // position: q_full 0, final 1, k_full 2.., k_free, v_full, v_free, s_full,
+  // p_full, pv_done (two each for the last three).
+  struct Bars {
+    uint64_t q_full, final;
+    uint64_t k_full[C::kKStages], k_free[C::kKStages];
+    uint64_t v_full[C::kVStages], v_free[C::kVStages];
+    uint64_t s_full[2], p_full[2], pv_done[2];
+  };
+  __shared__ Bars bars;
+  uint64_t& bar_q_full = bars.q_full;
+  uint64_t& bar_final = bars.final;
+  uint64_t(&bar_k_full)[C::kKStages] = bars.k_full;
+  uint64_t(&bar_k_free)[C::kKStages] = bars.k_free;
+  uint64_t(&bar_v_full)[C::kVStages] = bars.v_full;
+  uint64_t(&bar_v_free)[C::kVStages] = bars.v_free;
+  uint64_t(&bar_s_full)[2] = bars.s_full;
+  uint64_t(&bar_p_full)[2] = bars.p_full;
+  uint64_t(&bar_pv_done)[2] = bars.pv_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ WorkItem s_item;
@@ -393,7 +409,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (tid == 0 && s_abort) atomicOr(args.g.status, kStatusTimeout);
+  if (tid == 0 && s_abort) {
+    const uint32_t a = static_cast<uint32_t>(s_abort) - 1u, base = smem_u32(&bars);
+    record_timeout(args.g.status, args.g.timeout_info, kTimeoutKernelFwd,
+                   a >= base && a < base + sizeof(Bars) ? (a - base) / 8 : 0xfffu);
+  }
 }
 
 template <int D>

@@ -21,7 +21,7 @@ struct PlanScalars {
   int32_t n_tiles;
   int32_t status;
   int32_t n_pairs;
-  int32_t pad;
+  int32_t timeout_info;   // record_timeout's word (0: no wait timed out)
 };
 
 struct PlanArgs {
@@ -68,6 +68,7 @@ struct AttnGeom {
   int32_t heads;
   int32_t n_items;          // work units (tiles or pairs) * heads
   int32_t* status;
+  int32_t* timeout_info;    // the plan's timeout record (PlanScalars::timeout_info)
   int32_t debug;            // MF_DEBUG_* flags of mf_debug_inject (0 in normal use)
 };
 

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kPlanThreads) pack_scan_kernel(PlanArgs a) {
     const bool same = x.n_packed == np && x.total_tokens == total && x.max_seqlen == s_maxlen &&
                       x.max_grid == s_maxgrid && x.n_tiles == n_tiles && x.n_pairs == n_pairs;
     a.scalars->status = same ? 0 : kStatusPlan;
+    a.scalars->timeout_info = 0;
   }
 }
 

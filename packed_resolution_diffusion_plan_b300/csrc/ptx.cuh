@@ -75,7 +75,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed.  Returns false
 // (without waiting further) once the CTA abort flag is up, and raises that
-// flag itself after kWaitTimeoutNs.  Callers leave their loop on false.
+// flag itself after kWaitTimeoutNs, setting it to the timed-out barrier's
+// shared-memory address + 1.  Callers leave their loop on false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
@@ -84,11 +85,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if ((it & 63u) == 0u) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        *abort_flag = 1;
+        *abort_flag = static_cast<int>(smem_u32(bar)) + 1;
         return false;
       }
     }
   }
+}
+
+// A CTA gave up a wait: raise the timeout status and count the CTA in the
+// plan's timeout record (kernel << 28 | barrier of the first timeout << 16 |
+// CTAs that timed out, saturating at 0xffff).  `barrier` is the index of the
+// timed-out barrier in the kernel's barrier block (0xfff: unknown).
+static __device__ __noinline__ void record_timeout(int32_t* status, int32_t* info, uint32_t kernel, uint32_t barrier) {
+  atomicOr(status, kStatusTimeout);
+  unsigned int* w = reinterpret_cast<unsigned int*>(info);
+  unsigned int old = *w, assumed;
+  do {
+    assumed = old;
+    const unsigned int n = assumed & 0xffffu;
+    const unsigned int next = assumed == 0u ? ((kernel << 28) | ((barrier & 0xfffu) << 16) | 1u)
+                                            : ((assumed & 0xffff0000u) | (n < 0xffffu ? n + 1u : n));
+    old = atomicCAS(w, assumed, next);
+  } while (old != assumed);
 }
 
 // ---------------------------------------------------------------- fences

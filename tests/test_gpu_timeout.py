@@ -6,6 +6,7 @@ kernel must then leave every loop, free its TMEM and exit with the timeout
 status, which mf_check reports as MF_ERR_TIMEOUT and clears; the next normal
 call on the same context must produce correct results.
 """
+import re
 import time
 
 import pytest
@@ -27,13 +28,20 @@ def _inputs():
     return wl, plan, q, k, v, do
 
 
-def _expect_timeout(plan):
+def _expect_timeout(plan, kernel, n_ctas):
+    """MF_ERR_TIMEOUT, with the record naming the kernel, a barrier of its
+    barrier block and every CTA (each one's loads were dropped)."""
     t0 = time.time()
     with pytest.raises(mf.MfError) as ei:
         mf.check(plan)
     assert ei.value.code == "MF_ERR_TIMEOUT"
     assert time.time() - t0 < 60.0
-    mf.check(plan)  # the status word was cleared
+    m = re.search(r"timed out in (\w+): first at barrier (\d+), (\d+) CTA", str(ei.value))
+    assert m, str(ei.value)
+    assert m.group(1) == kernel
+    assert int(m.group(2)) < 32
+    assert int(m.group(3)) == n_ctas
+    mf.check(plan)  # the status word and the record were cleared
 
 
 def test_fwd_dropped_loads_time_out_then_recover():
@@ -43,7 +51,7 @@ def test_fwd_dropped_loads_time_out_then_recover():
         mf.attn_fwd(q, k, v, plan)
     finally:
         mf.debug_inject(0)
-    _expect_timeout(plan)
+    _expect_timeout(plan, "attn_fwd_kernel", plan.n_pairs * q.shape[1])
     o, lse = mf.attn_fwd(q, k, v, plan)
     mf.check(plan)
     ref = oracle.pack_plan(wl.samples)
@@ -61,7 +69,7 @@ def test_bwd_dropped_loads_time_out_then_recover():
         mf.attn_bwd(q, k, v, o, lse, do, plan)
     finally:
         mf.debug_inject(0)
-    _expect_timeout(plan)
+    _expect_timeout(plan, "bwd_main_kernel", plan.n_tiles * q.shape[1])
     dq, dk, dv = mf.attn_bwd(q, k, v, o, lse, do, plan)
     mf.check(plan)
     ref = oracle.pack_plan(wl.samples)
