@@ -120,6 +120,17 @@ def _stream_ptr(stream, device):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _workspace(nbytes: int, device, stream):
+    """A device scratch buffer for a call enqueued on `stream`.  It is
+    allocated on torch's current stream; when the call runs on another one,
+    the buffer is tied to that stream too, so that the caching allocator does
+    not hand it out again while the call's kernels may still use it."""
+    ws = torch.empty(max(256, int(nbytes)), dtype=torch.uint8, device=device)
+    if stream is not None and stream != torch.cuda.current_stream(ws.device):
+        ws.record_stream(stream)
+    return ws
+
+
 def _samples_array(samples):
     arr = (MfSample * max(1, len(samples)))()
     for i, smp in enumerate(samples):
@@ -191,7 +202,7 @@ def pack_plan(samples, token_budget: int = 0, head_dim: int = 128, rope_theta: f
     nbytes = ctypes.c_size_t(0)
     _raise(L.mf_pack_plan_workspace_size(arr, len(samples), int(token_budget), int(head_dim), int(rope_axes),
                                          ctypes.byref(nbytes)), "mf_pack_plan_workspace_size")
-    ws = torch.empty(max(256, nbytes.value), dtype=torch.uint8, device=device)
+    ws = _workspace(nbytes.value, device, stream)
     raw = MfPlan()
     _raise(L.mf_pack_plan(arr, len(samples), int(token_budget), int(head_dim), int(rope_axes), float(rope_theta),
                           ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.byref(raw),
@@ -226,7 +237,7 @@ def attn_fwd(q, k, v, plan: Plan, softmax_scale: float = 0.0, out=None, lse=None
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
     if workspace is None:
-        workspace = torch.empty(max(256, fwd_workspace_bytes(T, H, D)), dtype=torch.uint8, device=q.device)
+        workspace = _workspace(fwd_workspace_bytes(T, H, D), q.device, stream)
     _raise(lib().mf_attn_fwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
                              ctypes.c_void_p(v.data_ptr()), ctypes.byref(plan.raw), H, D,
                              float(softmax_scale), ctypes.c_void_p(workspace.data_ptr()),
@@ -250,7 +261,7 @@ def attn_bwd(q, k, v, o, lse, do, plan: Plan, softmax_scale: float = 0.0, worksp
     T, H, D = q.shape
     nbytes = bwd_workspace_bytes(T, H, D)
     if workspace is None:
-        workspace = torch.empty(max(256, nbytes), dtype=torch.uint8, device=q.device)
+        workspace = _workspace(nbytes, q.device, stream)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
@@ -281,7 +292,7 @@ def attn_bwd_rotated(fwd_workspace, v, o, lse, do, plan: Plan, softmax_scale: fl
     if not (fwd_workspace.is_cuda and fwd_workspace.dtype == torch.uint8 and fwd_workspace.is_contiguous()):
         raise ValueError("fwd_workspace must be the forward's contiguous uint8 CUDA workspace")
     if workspace is None:
-        workspace = torch.empty(max(256, bwd_rotated_workspace_bytes(T, H, D)), dtype=torch.uint8, device=v.device)
+        workspace = _workspace(bwd_rotated_workspace_bytes(T, H, D), v.device, stream)
     dq = torch.empty_like(v) if dq is None else dq
     dk = torch.empty_like(v) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -356,7 +367,7 @@ def attn_fwd_qkv(qkv, plan: Plan, heads: int, softmax_scale: float = 0.0, out=No
     out = torch.empty((T, heads, D), dtype=torch.bfloat16, device=qkv.device) if out is None else out
     lse = torch.empty((heads, T), dtype=torch.float32, device=qkv.device) if lse is None else lse
     if workspace is None:
-        workspace = torch.empty(max(256, fwd_workspace_bytes(T, heads, D)), dtype=torch.uint8, device=qkv.device)
+        workspace = _workspace(fwd_workspace_bytes(T, heads, D), qkv.device, stream)
     _raise(lib().mf_attn_fwd_qkv(ctypes.c_void_p(qkv.data_ptr()), ctypes.byref(plan.raw), heads, D,
                                  float(softmax_scale), ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                                  ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
