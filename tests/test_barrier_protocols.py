@@ -45,8 +45,9 @@ class Overrun(AssertionError):
     pass
 
 
-def _bwd_roles(n_q, fixed):
-    """Generators yielding ('wait', bar, phase), ('arrive', bar),
+def _bwd_roles(n_q, fixed, head_dim=128):
+    """head_dim 64 has no reducer: dQ leaves by atomics, q_free takes the
+    MMA's arrival alone and staging is a no-op.  Generators yielding ('wait', bar, phase), ('arrive', bar),
     ('commit', bar) or ('tma', bar)."""
 
     def producer():
@@ -108,6 +109,8 @@ def _bwd_roles(n_q, fixed):
             yield ("arrive", "dq_free")
 
         def dq_stage(t):
+            if head_dim != 128:
+                return
             if cw == 0 and t >= 1:
                 yield ("wait", "stage_free", t - 1)
             if fixed and cw == 1 and t >= 1:
@@ -133,13 +136,16 @@ def _bwd_roles(n_q, fixed):
             yield ("wait", "fin", 0)
         return body()
 
-    return {"producer": producer(), "mma": mma(), "reducer": reducer(), "row": row_warp(),
-            "wg0": compute(0), "wg1": compute(1)}
+    roles = {"producer": producer(), "mma": mma(), "row": row_warp(), "wg0": compute(0), "wg1": compute(1)}
+    if head_dim == 128:
+        roles["reducer"] = reducer()
+    return roles
 
 
-def _bwd_barriers():
+def _bwd_barriers(head_dim=128):
+    nf = 2 if head_dim == 128 else 1
     counts = {"kv_full": 1, "fin": 1, "q_full0": 1, "q_full1": 1, "q_ready0": 1, "q_ready1": 1,
-              "q_free0": 2, "q_free1": 2, "do_full": 1, "do_free": 1, "s_full": 1, "p_ready": 2,
+              "q_free0": nf, "q_free1": nf, "do_full": 1, "do_free": 1, "s_full": 1, "p_ready": 2,
               "dp_full": 1, "ds_ready": 2, "a_free": 1, "dq_full": 1, "dq_free": 2, "stage_full0": 1,
               "stage_full1": 1, "stage_free": 1, "q_issued": 1}
     return {n: Barrier(n, c) for n, c in counts.items()}
@@ -210,14 +216,14 @@ def _fwd_barriers(k_stages=3, v_stages=2):
     return {n: Barrier(n, 1) for n in names}
 
 
-def run_schedule(n_q, seed, fixed=True, kernel="bwd", max_steps=200000):
+def run_schedule(n_q, seed, fixed=True, kernel="bwd", head_dim=128, max_steps=200000):
     """One random interleaving of `kernel`'s protocol over n_q Q tiles
     (backward) or n_q K/V tiles (forward).  Returns None when every role
     finished, or a string describing the deadlock; raises Overrun on a phase
     overrun."""
     rng = random.Random(seed)
     if kernel == "bwd":
-        bars, roles = _bwd_barriers(), _bwd_roles(n_q, fixed)
+        bars, roles = _bwd_barriers(head_dim), _bwd_roles(n_q, fixed, head_dim)
     else:
         bars, roles = _fwd_barriers(), _fwd_roles(n_q, random.Random(seed + 7919))
     nxt = {r: next(g) for r, g in roles.items()}
@@ -267,10 +273,11 @@ def run_schedule(n_q, seed, fixed=True, kernel="bwd", max_steps=200000):
     return None
 
 
+@pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("n_q", [1, 2, 3, 4, 5, 8])
-def test_bwd_protocol_never_overruns_or_deadlocks(n_q):
+def test_bwd_protocol_never_overruns_or_deadlocks(n_q, head_dim):
     for seed in range(300):
-        assert run_schedule(n_q, seed) is None, (n_q, seed)
+        assert run_schedule(n_q, seed, head_dim=head_dim) is None, (n_q, head_dim, seed)
 
 
 @pytest.mark.parametrize("n_kv", [1, 2, 3, 4, 5, 7])
