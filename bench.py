@@ -477,12 +477,27 @@ KERNEL_SOURCES = {
 }
 
 
-def kernel_source_hash(kernel):
+_CODE_TOKENS = None
+
+
+def code_only(text):
+    """C++/CUDA source without its comments, whitespace runs collapsed:
+    what the compiler sees, so that editing a comment keeps the hash."""
+    import re
+    global _CODE_TOKENS
+    if _CODE_TOKENS is None:
+        _CODE_TOKENS = re.compile(r'("(?:\\.|[^"\\])*")|/\*.*?\*/|//[^\n]*', re.S)
+    text = _CODE_TOKENS.sub(lambda m: m.group(1) or " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_hash(kernel, root=None):
+    """Hash of the code (comments excluded) of the files `kernel` is built from."""
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "packed_resolution_diffusion_plan_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(root or ROOT, "packed_resolution_diffusion_plan_b300", "csrc", f)) as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -5,12 +5,17 @@
 // MMDiT": the packed attention is trained, so its backward runs on the same
 // packs; the row log-sum-exp of the forward lets P be recomputed):
 //   P = exp(S - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
-//   dS = P * (dP - D), dq~ = s dS k~, dk~ = s dS^T q~, dq = R^T dq~, dk = R^T dk~.
+//   dS = P * (dP - D), dq = R^T (s dS R(k)), dk = R^T (s dS^T R(q)).
+// The logit operands are fp16 copies q~, k~ of R(q), R(k), one of them
+// carrying the factor s log2(e); dk~ = dS^T q~ and dq~ = dS k~ are taken back
+// by dk_mult and dq_mult (s and ln 2, swapped when q~ carries the factor).
 //
 // Three kernels:
 //   bwd_pre      D = rowsum(dO * O) (float32 [heads, T]); zero the float32 dQ
-//                accumulator; q~ = R(q) and k~ = s log2(e) R(k) as fp16
-//                [T, heads, D], rotated once per token.
+//                accumulator; unless the forward's copies are used
+//                (q~ = s log2(e) R(q), k~ = R(k)), q~ = R(q) and
+//                k~ = s log2(e) R(k) as fp16 [T, heads, D], rotated once per
+//                token.
 //   bwd_main     one CTA per (sample, head, 128-row K/V tile), streaming the
 //                sample's 128-row q~/dO tiles (a two-slot q~ ring, one dO
 //                slot).  Per Q tile i, five tcgen05 MMAs (TMEM columns:
@@ -18,7 +23,7 @@
 //                  S^T_i  = k~ q~_i^T        fp16, smem x smem -> A
 //                  dP^T_i = V dO_i^T         bf16, smem x smem -> B
 //                  dV    += P^T_i dO_i       bf16, P^T from TMEM (A) x smem
-//                  dk~   += dS^T_i q~_i      fp16, smem x smem
+//                  dk~   += dS^T_i q~_i      fp16, dS^T from TMEM (A) x smem
 //                  dQ_i   = dS_i k~          fp16, smem x smem -> B; with
 //                           head_dim 128 it is formed transposed (k~^T dS^T,
 //                           TMEM lane = dimension), so that a warp's stores
@@ -29,8 +34,9 @@
 //                  WG0, WG1  thread r owns K/V row r (TMEM lane r), WG c the
 //                            query columns 64c..64c+63: P^T = exp2(S^T - LSE2)
 //                            written back over its S^T columns as packed bf16,
-//                            dS^T = P^T * (dP^T - D) as fp16 into shared
-//                            memory; the dQ epilogue (TMEM -> staging tile,
+//                            dS^T = P^T * (dP^T - D) as fp16 into TMEM
+//                            (beside P^T, for dK) and shared memory (for
+//                            dQ); the dQ epilogue (TMEM -> staging tile,
 //                            half the tile each); at the end dV and R^T dk~
 //                  WG2       warp 8 TMA producer (q~ ring of two, one dO
 //                            slot), warp 9 TMEM owner and MMA issuer, warp
@@ -42,7 +48,7 @@
 //                            accumulator by one TMA reduce, so the compute
 //                            warps never wait on the reduction traffic; warp
 //                            11 the per-tile -LSE2 / -D rows
-//   bwd_dq       dq = R^T (s * accumulator) as bf16.
+//   bwd_dq       dq = R^T (dq_mult * accumulator) as bf16.
 #include "attn_common.cuh"
 
 namespace mf {
