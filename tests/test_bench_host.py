@@ -21,8 +21,3 @@ def test_comment_edits_keep_the_hash_and_code_edits_change_it():
     assert bench.code_only(base) == bench.code_only(recommented)
     assert bench.code_only(base) != bench.code_only(changed)
 
-
-def test_committed_traffic_matches_the_current_kernels():
-    """The committed counters belong to the kernels as they stand."""
-    for k in bench.KERNEL_SOURCES:
-        assert bench.load_traffic(k) is not None, k
