@@ -244,9 +244,11 @@ MF_API mf_status mf_attn_bwd_rotated(const void *fwd_workspace, size_t fwd_works
  * MF_NOALLOC_SCRATCH_BYTES array of device memory that the library reserves
  * on every GPU that loads it, held until the process exits.  It allocates
  * nothing itself.
- *   - The first call on a device looks up that array's device address (with
- *     the device current) and caches it; make that first call before any
- *     stream capture.
+ *   - A call looks up that array's device address on the current device
+ *     (a device reset reloads the library's GPU code, and the array may then
+ *     sit elsewhere) and caches it per device.  A call made while `stream`
+ *     is capturing uses the cached address instead, so make a first call on
+ *     each device before any stream capture.
  *   - Packs whose backward workspace (mf_attn_bwd_workspace_size) exceeds
  *     MF_NOALLOC_SCRATCH_BYTES return MF_ERR_UNSUPPORTED without launching;
  *     use mf_attn_bwd with a caller workspace for those.

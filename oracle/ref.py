@@ -33,6 +33,9 @@ What it computes, and where each step comes from:
   softmax(s * q~ k~^T) v per sample and head, with s = 1/sqrt(head_dim) unless
   given; the backward is the exact gradient of that definition with respect
   to the un-rotated q, k and v.
+* ``attn_rows`` / ``attn_bwd_rows`` -- the same forward and backward for
+  selected rows of one head, row by row (O(L D) per row once a sample's row
+  statistics are known), so that full-size packs can be checked.
 * ``cfg_combine`` -- classifier-free guidance over a pack whose samples come
   in (conditional, unconditional) pairs (review, section on CFG: the two
   branches run in one packed forward).  The pages do not print the
@@ -276,7 +279,8 @@ def attn_rows(q, k, v, cu_seqlens, pos, rows, head: int, softmax_scale: float = 
     """O and LSE of selected query rows of one head, one row at a time.
 
     For full-size packs: each row touches only its own sample's keys, so it
-    costs O(L * D).  Returns (O [len(rows), D], LSE [len(rows)]).
+    costs O(L * D) (the sample's rotated keys are formed once for all of its
+    requested rows).  Returns (O [len(rows), D], LSE [len(rows)]).
     """
     q = np.asarray(q[:, head, :], dtype=np.float64)[:, None, :]
     k = np.asarray(k[:, head, :], dtype=np.float64)[:, None, :]
@@ -284,21 +288,103 @@ def attn_rows(q, k, v, cu_seqlens, pos, rows, head: int, softmax_scale: float = 
     D = q.shape[2]
     s = softmax_scale if softmax_scale > 0 else default_scale(D)
     cu = np.asarray(cu_seqlens)
+    rows = [int(r) for r in rows]
     O = np.zeros((len(rows), D))
     LSE = np.zeros(len(rows))
-    for n, r in enumerate(rows):
-        i = int(np.searchsorted(cu, r, side="right") - 1)
+    sample = [int(np.searchsorted(cu, r, side="right") - 1) for r in rows]
+    for i in sorted(set(sample)):
         a, b = int(cu[i]), int(cu[i + 1])
-        fq = None if frame is None else frame[r:r + 1]
         fk = None if frame is None else frame[a:b]
-        qr = rope(q[r:r + 1], pos[r:r + 1], theta, frame=fq, rope_axes=rope_axes)[0, 0]
         kr = rope(k[a:b], pos[a:b], theta, frame=fk, rope_axes=rope_axes)[:, 0, :]
-        srow = s * (kr @ qr)
-        m = srow.max()
-        lse = m + math.log(np.exp(srow - m).sum())
-        O[n] = np.exp(srow - lse) @ v[a:b]
-        LSE[n] = lse
+        for n, r in enumerate(rows):
+            if sample[n] != i:
+                continue
+            fq = None if frame is None else frame[r:r + 1]
+            qr = rope(q[r:r + 1], pos[r:r + 1], theta, frame=fq, rope_axes=rope_axes)[0, 0]
+            srow = s * (kr @ qr)
+            m = srow.max()
+            lse = m + math.log(np.exp(srow - m).sum())
+            O[n] = np.exp(srow - lse) @ v[a:b]
+            LSE[n] = lse
     return O, LSE
+
+
+def attn_bwd_rows(q, k, v, do, cu_seqlens, pos, head: int, q_rows=(), kv_rows=(), softmax_scale: float = 0.0,
+                  theta: float = 10000.0, frame=None, rope_axes: int = 2, block: int = 1024):
+    """dQ of selected query rows and dK, dV of selected key rows of one head.
+
+    The same gradients as ``attn_bwd`` (the exact gradient of per-sample
+    softmax(s q~ k~^T) v with respect to the un-rotated q, k, v), taken one
+    row at a time so that full-size packs stay affordable:
+
+      * the sample's row statistics first: for every query row r of a sample
+        that holds a requested row, LSE_r = logsumexp_j S[r, j],
+        O_r = sum_j exp(S[r, j] - LSE_r) v_j and D_r = dO_r . O_r
+        (S = s q~ k~^T; the rows are visited ``block`` at a time only to bound
+        memory, each row on its own);
+      * query row r:  dS[r, :] = P[r, :] (dP[r, :] - D_r) with
+        P[r, j] = exp(S[r, j] - LSE_r) and dP[r, j] = dO_r . v_j;
+        dq_r = R^T (s sum_j dS[r, j] k~_j);
+      * key row c:    dv_c = sum_r P[r, c] dO_r;
+        dS[:, c] = P[:, c] (dP[:, c] - D);  dk_c = R^T (s sum_r dS[r, c] q~_r).
+
+    Each requested row costs O(L D) once the statistics are known.  D_r here
+    uses this oracle's own O (the library's backward receives the forward's
+    O; the two agree within the forward's tolerance).  Returns (dq
+    [len(q_rows), D], dk [len(kv_rows), D], dv [len(kv_rows), D]) in float64.
+    """
+    q = np.asarray(q[:, head, :], dtype=np.float64)
+    k = np.asarray(k[:, head, :], dtype=np.float64)
+    v = np.asarray(v[:, head, :], dtype=np.float64)
+    do = np.asarray(do[:, head, :], dtype=np.float64)
+    D = q.shape[1]
+    s = softmax_scale if softmax_scale > 0 else default_scale(D)
+    cu = np.asarray(cu_seqlens)
+    pos = np.asarray(pos)
+    q_rows = [int(r) for r in q_rows]
+    kv_rows = [int(r) for r in kv_rows]
+    dq = np.zeros((len(q_rows), D))
+    dk = np.zeros((len(kv_rows), D))
+    dv = np.zeros((len(kv_rows), D))
+
+    def sample_of(r):
+        return int(np.searchsorted(cu, r, side="right") - 1)
+
+    def rot(x, a, b, inverse=False):
+        fr = None if frame is None else np.asarray(frame)[a:b]
+        return rope(x[:, None, :], pos[a:b], theta, inverse=inverse, frame=fr, rope_axes=rope_axes)[:, 0, :]
+
+    for i in sorted({sample_of(r) for r in q_rows + kv_rows}):
+        a, b = int(cu[i]), int(cu[i + 1])
+        qr, kr = rot(q[a:b], a, b), rot(k[a:b], a, b)
+        vs, dos = v[a:b], do[a:b]
+        L = b - a
+        lse = np.zeros(L)
+        dsum = np.zeros(L)
+        for r0 in range(0, L, block):
+            S = s * (qr[r0:r0 + block] @ kr.T)
+            m = S.max(axis=1, keepdims=True)
+            E = np.exp(S - m)
+            z = E.sum(axis=1, keepdims=True)
+            lse[r0:r0 + block] = (m + np.log(z))[:, 0]
+            O = (E / z) @ vs
+            dsum[r0:r0 + block] = (dos[r0:r0 + block] * O).sum(axis=1)
+        for n, r in enumerate(q_rows):
+            if sample_of(r) != i:
+                continue
+            j = r - a
+            P = np.exp(s * (kr @ qr[j]) - lse[j])
+            dS = P * (vs @ dos[j] - dsum[j])
+            dq[n] = rot((s * (dS @ kr))[None, :], r, r + 1, inverse=True)[0]
+        for n, c in enumerate(kv_rows):
+            if sample_of(c) != i:
+                continue
+            j = c - a
+            P = np.exp(s * (qr @ kr[j]) - lse)
+            dv[n] = P @ dos
+            dS = P * (dos @ vs[j] - dsum)
+            dk[n] = rot((s * (dS @ qr))[None, :], c, c + 1, inverse=True)[0]
+    return dq, dk, dv
 
 
 def cfg_combine(o, cu_seqlens, pos, guidance: float):

@@ -7,9 +7,10 @@
 // backward: for example an engine plugin whose execute step is forbidden to
 // allocate, a runtime that hands all device memory to its own pool at
 // start-up and has none left to give, or a latency-critical loop that must
-// not call cudaMalloc because it can synchronize the device.  For them this file keeps a fixed scratch
-// array in device memory, reserved when the library's GPU code is loaded and
-// held by every GPU that loads it until the process exits.
+// not call cudaMalloc because it can synchronize the device.  For them this
+// file keeps a fixed scratch array in device memory, reserved when the
+// library's GPU code is loaded and held by every GPU that loads it until the
+// process exits.
 #include <atomic>
 
 #include "../../include/mf.h"
@@ -25,14 +26,20 @@ constexpr int kMaxDevices = 64;
 std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 // Device address of g_bwd_scratch on the current device.  The host-side name
-// of the array is only a stand-in, so the address is looked up once per
-// device (with that device current) and cached.
-mf_status scratch_address(void** out) {
+// of the array is only a stand-in, so the address is looked up with the
+// device current.  A call outside stream capture looks it up every time (a
+// device reset reloads the module, and the array may then sit elsewhere) and
+// caches it per device; a call made while `stream` is capturing takes the
+// cached address, or looks it up if the device has none yet.
+mf_status scratch_address(cudaStream_t stream, void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return MF_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MF_ERR_UNSUPPORTED;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return MF_ERR_CUDA;
+  void* p = cap == cudaStreamCaptureStatusNone ? nullptr : g_scratch_addr[dev].load(std::memory_order_acquire);
   if (p == nullptr) {
     e = cudaGetSymbolAddress(&p, g_bwd_scratch);
     if (e != cudaSuccess || p == nullptr) return MF_ERR_CUDA;
@@ -56,7 +63,7 @@ extern "C" mf_status mf_attn_bwd_noalloc(const void* q, const void* k, const voi
   if (st != MF_OK) return st;
   if (need > kScratchBytes) return MF_ERR_UNSUPPORTED;  // pack too large for the fixed scratch
   void* scratch = nullptr;
-  if ((st = scratch_address(&scratch)) != MF_OK) return st;
+  if ((st = scratch_address(static_cast<cudaStream_t>(stream), &scratch)) != MF_OK) return st;
   // The backward's first kernel overwrites D and the rotated copies and zeroes
   // the accumulator, so whatever an earlier call left in the array does not
   // leak into this one.

@@ -145,3 +145,51 @@ def test_bwd_full_size_per_sample(name, samples_idx, rotated):
             assert_close(f"dV[{name},s{si},h{h}]", dv_c[a:b, hs], rv, "grad")
             assert_close(f"dK[{name},s{si},h{h}]", dk_c[a:b, hs], rk, "grad")
             assert_close(f"dQ[{name},s{si},h{h}]", dq_c[a:b, hs], rq, "grad")
+
+
+def _edge_rows(a, b, rng, n_random):
+    """Rows of sample [a, b): its first and last rows, both sides of every
+    fourth 128-row tile edge, the last tile's first row and a few random rows."""
+    rows = {a, a + 1, b - 2, b - 1, b - 1 - (b - a - 1) % 128}
+    for e in range(a + 128, b, 512):
+        rows |= {e - 1, e}
+    rows |= set(int(x) for x in rng.integers(a, b, size=n_random))
+    return sorted(r for r in rows if a <= r < b)
+
+
+@pytest.mark.parametrize("name,samples_idx", [("native_res_32k", [0, 3]), ("extreme_aspect", [2])])
+def test_bwd_full_size_long_samples_rows(name, samples_idx):
+    """The long samples that dominate the benched fwd+bwd packs (10,749 and
+    10,577 tokens of the training pack, 16,640 of the extreme-aspect pack: up
+    to 130 K/V tiles whose dQ partials meet in one accumulator row), in the
+    bench's launch configuration, through both backward entry points, on every
+    head: sampled query rows (dQ) and key rows (dK, dV) against the row-wise
+    oracle, which takes each sample's full-row statistics."""
+    wl = synth.WORKLOADS[name]()
+    t = synth.draw_tensors(wl, with_grad=True)
+    plan = mf.pack_plan(wl.samples, token_budget=wl.token_budget, head_dim=wl.head_dim)
+    T = plan.total_tokens
+    q, k, v, do = (t[n][:T].cuda() for n in ("q", "k", "v", "do"))
+    wsf = torch.empty(mf.fwd_workspace_bytes(T, wl.heads, wl.head_dim), dtype=torch.uint8, device="cuda")
+    o, lse = mf.attn_fwd(q, k, v, plan, workspace=wsf)
+    got = {"rotated": mf.attn_bwd_rotated(wsf, v, o, lse, do, plan),
+           "plain": mf.attn_bwd(q, k, v, o, lse, do, plan)}
+    mf.check(plan)
+    got = {e: [to64(x) for x in g] for e, g in got.items()}
+    for g in got.values():
+        assert all(np.all(np.isfinite(x)) for x in g)
+    ref = oracle.pack_plan(wl.samples, wl.token_budget)
+    cu, pos = ref["cu_seqlens"], ref["pos"]
+    rng = np.random.default_rng(1)
+    q_rows, kv_rows = [], []
+    for si in samples_idx:
+        a, b = int(cu[si]), int(cu[si + 1])
+        q_rows += _edge_rows(a, b, rng, 6)
+        kv_rows += _edge_rows(a, b, rng, 6)
+    qn, kn, vn, gn = (t[n].float().numpy() for n in ("q", "k", "v", "do"))
+    for h in range(wl.heads):
+        rq, rk, rv = oracle.attn_bwd_rows(qn, kn, vn, gn, cu, pos, h, q_rows=q_rows, kv_rows=kv_rows)
+        for e, (dq, dk, dv) in got.items():
+            assert_close(f"dQ[{name},{e},h{h}]", dq[q_rows, h], rq, "grad")
+            assert_close(f"dK[{name},{e},h{h}]", dk[kv_rows, h], rk, "grad")
+            assert_close(f"dV[{name},{e},h{h}]", dv[kv_rows, h], rv, "grad")

@@ -581,3 +581,50 @@ def test_bwd_zero_rotation_equals_torch_autograd():
         out.backward(torch.from_numpy(g[a:b]).transpose(0, 1))
         for ref, mine in ((tq, dq), (tk, dk), (tv, dv)):
             assert np.abs(ref.grad.transpose(0, 1).numpy() - mine[a:b]).max() < 1e-12
+
+
+def test_attn_bwd_rows_matches_bwd():
+    """The row-wise backward gives attn_bwd's gradients row by row (tiny pack,
+    a ragged pack with text-only and one-token samples, an edit pack with
+    (h, w, f) RoPE and a non-default scale); a small block size exercises the
+    statistics pass over several row blocks and a ragged last block."""
+    cases = []
+    _, p, t = _tiny_inputs(3)
+    cases.append((p, t["q"], t["k"], t["v"], t["do"], {}, 0.0))
+    samples = [(5, 32, 48), (9, 0, 0), (1, 16, 16), (0, 48, 16)]
+    p = oracle.pack_plan(samples)
+    q, k, v, g = _rand_qkv(p["total_tokens"], 2, 32, 17)
+    cases.append((p, q, k, v, g, {}, 0.3))
+    p = oracle.pack_plan([(4, 32, 32, 2), (3, 16, 48)])
+    q, k, v, g = _rand_qkv(p["total_tokens"], 2, 32, 18)
+    cases.append((p, q, k, v, g, {"frame": p["frame"], "rope_axes": 3}, 0.0))
+    for p, q, k, v, g, ro, sc in cases:
+        cu, pos = p["cu_seqlens"], p["pos"]
+        O, L = oracle.attn_fwd(q, k, v, cu, pos, softmax_scale=sc, **ro)
+        dq, dk, dv = oracle.attn_bwd(q, k, v, O, L, g, cu, pos, softmax_scale=sc, **ro)
+        T = p["total_tokens"]
+        rows = sorted({0, 1, T // 3, T // 2, T - 2, T - 1} | {int(c) for c in cu[1:-1]})
+        for h in range(q.shape[1]):
+            rq, rk, rv = oracle.attn_bwd_rows(q, k, v, g, cu, pos, h, q_rows=rows, kv_rows=rows[::-1],
+                                              softmax_scale=sc, block=7, **ro)
+            assert np.abs(rq - dq[rows, h]).max() < 1e-12
+            assert np.abs(rk - dk[rows[::-1], h]).max() < 1e-12
+            assert np.abs(rv - dv[rows[::-1], h]).max() < 1e-12
+
+
+def test_attn_bwd_rows_finite_differences():
+    """Single entries of the row-wise gradients against central finite
+    differences of the forward (independently of attn_bwd)."""
+    _, p, t = _tiny_inputs(4)
+    q, k, v, g = t["q"], t["k"], t["v"], t["do"]
+    cu, pos = p["cu_seqlens"], p["pos"]
+    eps = 1e-6
+    for tok, h, d in [(3, 0, 1), (30, 1, 40), (90, 0, 63), (120, 1, 17)]:
+        rq, rk, rv = oracle.attn_bwd_rows(q, k, v, g, cu, pos, h, q_rows=[tok], kv_rows=[tok])
+        for x, got in ((q, rq[0, d]), (k, rk[0, d]), (v, rv[0, d])):
+            e = np.zeros_like(x)
+            e[tok, h, d] = 1.0
+            args_p = [x + eps * e if y is x else y for y in (q, k, v)]
+            args_m = [x - eps * e if y is x else y for y in (q, k, v)]
+            fd = (_loss(*args_p, g, p) - _loss(*args_m, g, p)) / (2 * eps)
+            assert abs(fd - got) <= 1e-6 * max(1.0, abs(fd)), (tok, h, d, fd, got)
