@@ -2,9 +2,8 @@
 """Benchmark of the packed native-resolution attention hot path on B300.
 
 One step = the whole path over one synthetic pack: mf_pack_plan (device
-scan, per-token ids, RoPE table), mf_attn_fwd, and the backward from the
-rotated Q/K copies the forward left in its workspace (mf_attn_bwd_rotated;
-`--bwd plain` runs mf_attn_bwd, which rotates Q and K again).  Throughput is
+scan, per-token ids, RoPE table), mf_attn_fwd and mf_attn_bwd (forward-only
+workloads: plan and forward).  Throughput is
 reported as fwd+bwd TFLOP/s with FLOPs = 4*heads*head_dim*sum(L_i^2) forward
 and 2.5x that backward (algorithmic: only the per-sample blocks count).
 
@@ -60,8 +59,6 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-threads", type=int, default=0, help="BLAS threads of the oracle baseline (0: all)")
     ap.add_argument("--e2e-steps", type=int, default=8)
-    ap.add_argument("--bwd", choices=["rotated", "plain"], default="rotated",
-                    help="backward entry: from the forward's rotated copies, or from Q and K")
     return ap.parse_args()
 
 
@@ -300,17 +297,12 @@ def run_mf(args):
     o = torch.empty_like(q)
     lse = torch.empty((H, T), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    rotated = args.bwd == "rotated"
-    ws_bytes = mf.bwd_rotated_workspace_bytes(T, H, D) if rotated else mf.bwd_workspace_bytes(T, H, D)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws = torch.empty(mf.bwd_workspace_bytes(T, H, D), dtype=torch.uint8, device=dev)
     ws_fwd = torch.empty(mf.fwd_workspace_bytes(T, H, D), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def backward(q, k, v, o, lse, do, plan, ws, ws_fwd, dq, dk, dv, stream=None):
-        if rotated:
-            mf.attn_bwd_rotated(ws_fwd, v, o, lse, do, plan, workspace=ws, dq=dq, dk=dk, dv=dv, stream=stream)
-        else:
-            mf.attn_bwd(q, k, v, o, lse, do, plan, workspace=ws, dq=dq, dk=dk, dv=dv, stream=stream)
+    def backward(q, k, v, o, lse, do, plan, ws, dq, dk, dv, stream=None):
+        mf.attn_bwd(q, k, v, o, lse, do, plan, workspace=ws, dq=dq, dk=dk, dv=dv, stream=stream)
 
     def step(ev=None):
         plan = mf.pack_plan(wl.samples, token_budget=wl.token_budget, head_dim=D, device=dev,
@@ -322,7 +314,7 @@ def run_mf(args):
             return plan
         if ev is not None:
             mf.record_main_kernel(ev[2], ev[3])
-        backward(q, k, v, o, lse, do, plan, ws, ws_fwd, dq, dk, dv)
+        backward(q, k, v, o, lse, do, plan, ws, dq, dk, dv)
         return plan
 
     # Each step plans anew, and every plan carries its own status word: check
@@ -408,7 +400,7 @@ def run_mf(args):
                              rope_axes=wl.rope_axes, stream=s_cmp)
             mf.attn_fwd(b["q"], b["k"], b["v"], p, out=b["o"], lse=b["lse"], workspace=b["wsf"], stream=s_cmp)
             if not fwd_only:
-                backward(b["q"], b["k"], b["v"], b["o"], b["lse"], b["do"], p, b["ws"], b["wsf"],
+                backward(b["q"], b["k"], b["v"], b["o"], b["lse"], b["do"], p, b["ws"],
                          b["dq"], b["dk"], b["dv"], stream=s_cmp)
             ev_cmp[j].record(s_cmp)
             e2e_plans.append(p)
@@ -471,13 +463,11 @@ def run_mf(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "precision": "bf16 inputs/outputs; tcgen05 MMAs with fp32 accumulation (logit products on fp16 "
-                     "copies of the rotated Q/K rows, P*V and dO products in bf16)",
+                     "rotated Q/K rows, P*V and dO products in bf16)",
         "config": {"workload": f"{wl.name} seed {wl.seed}", "samples": [list(x) for x in wl.samples],
                    "seq_lens": lens, "total_tokens": T, "heads": H, "head_dim": D,
                    "token_budget": wl.token_budget, "fwd_tflop": fwd_flop / 1e12, "bwd_tflop": bwd_flop / 1e12,
-                   "step": "pack plan + forward" if fwd_only else "pack plan + forward + backward" + (
-                       " (the backward reads the forward's rotated Q/K copies)" if rotated else
-                       " (the backward rotates Q and K again)"),
+                   "step": "pack plan + forward" if fwd_only else "pack plan + forward + backward",
                    "l2": (f"flushed: a 512 MB write between timed steps (Q/K/V/O are {T * H * D * 2 / 1e6:.0f} MB "
                           "each), each step timed on its own" if flush is not None else
                           f"no flush: Q/K/V/dO/O are {T * H * D * 2 / 1e6:.0f} MB each (> 126 MB L2)"),

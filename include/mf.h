@@ -44,10 +44,13 @@
  *   - softmax_scale <= 0 selects 1/sqrt(head_dim).
  *   - Precision: Q, K, V, O and the gradients are bf16 with fp32
  *     accumulation.  The logit product R(Q) R(K)^T is computed from fp16
- *     copies of the rotated rows (R(Q) pre-multiplied by softmax_scale *
- *     log2 e), whose finer significand keeps the rotation's rounding error
- *     8x below bf16's; a rotated value beyond the fp16 range (65504) is
- *     reported as MF_ERR_RANGE by mf_check.
+ *     rotated rows (R(Q) pre-multiplied by softmax_scale * log2 e), whose
+ *     finer significand keeps the rotation's rounding error 8x below bf16's.
+ *     Domain: every rotated, scaled value must stay within the fp16 range
+ *     (|s log2(e) R(q)|, |R(k)| <= 65504); a value beyond it is reported as
+ *     MF_ERR_RANGE by mf_check, never saturated silently.
+ *   - Samples are independent for any input: no value of one sample, finite
+ *     or not, reaches another sample's outputs.
  *   - head_dim must be 64 or 128 (MF_ERR_UNSUPPORTED otherwise).
  */
 #ifndef MF_H_
@@ -159,9 +162,9 @@ MF_API mf_status mf_pack_plan(const mf_sample *samples, int32_t n_samples, int32
                        int32_t head_dim, int32_t rope_axes, float rope_theta, void *workspace,
                        size_t workspace_bytes, mf_plan *plan_out, void *stream);
 
-/* Bytes of device workspace mf_attn_fwd needs: fp16 rotated copies
- * s log2(e) R(Q) and R(K) [total_tokens, heads, head_dim] (each section
- * 256-byte aligned). */
+/* Bytes of device workspace mf_attn_fwd needs: an fp16 rotated copy R(K)
+ * [total_tokens, heads, head_dim] (the streamed operand of the logit
+ * product) and the attention kernel's 256-byte work counter. */
 MF_API mf_status mf_attn_fwd_workspace_size(int32_t total_tokens, int32_t heads, int32_t head_dim,
                                             size_t *bytes);
 
@@ -171,7 +174,9 @@ MF_API mf_status mf_attn_fwd_workspace_size(int32_t total_tokens, int32_t heads,
  *   q, k, v     device bf16 [plan->total_tokens, heads, head_dim]
  *   workspace   device memory of mf_attn_fwd_workspace_size bytes, 256-byte
  *               aligned (contents on entry are ignored; a first kernel writes
- *               the rotated copies that the attention kernel streams)
+ *               the rotated K copy that the attention kernel streams, while
+ *               each Q tile is rotated in the attention kernel's prologue and
+ *               never written back)
  *   o           device bf16, same shape (written)
  *   lse         device float32 [heads, plan->total_tokens] (written)
  * Errors: MF_ERR_INVALID_ARG (null/misaligned pointer, heads < 1, head_dim
@@ -184,8 +189,9 @@ MF_API mf_status mf_attn_fwd(const void *q, const void *k, const void *v, const 
 
 /* Bytes of device workspace mf_attn_bwd needs: float32 row dots
  * D = rowsum(dO * O) [heads, total_tokens], a float32 dQ accumulator
- * [total_tokens, heads, head_dim] and fp16 rotated copies R(Q), s log2(e) R(K)
- * of the same shape (each section 256-byte aligned). */
+ * [total_tokens, heads, head_dim], an fp16 rotated copy s log2(e) R(Q) of the
+ * same shape (the streamed operand of the backward's logit product) and the
+ * attention kernel's 256-byte work counter (each section 256-byte aligned). */
 MF_API mf_status mf_attn_bwd_workspace_size(int32_t total_tokens, int32_t heads, int32_t head_dim,
                                      size_t *bytes);
 
@@ -196,40 +202,15 @@ MF_API mf_status mf_attn_bwd_workspace_size(int32_t total_tokens, int32_t heads,
  *   q, k, v, o, dout  device bf16 [total_tokens, heads, head_dim]
  *   lse               device float32 [heads, total_tokens] from mf_attn_fwd
  *   workspace         device memory of mf_attn_bwd_workspace_size bytes,
- *                     256-byte aligned (contents on entry are ignored)
+ *                     256-byte aligned (contents on entry are ignored; each
+ *                     K tile is rotated in the attention kernel's prologue
+ *                     and never written back)
  *   dq, dk, dv        device bf16 [total_tokens, heads, head_dim] (written)
  * Errors as mf_attn_fwd, plus a short workspace (MF_ERR_INVALID_ARG). */
 MF_API mf_status mf_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                       const float *lse, const void *dout, const mf_plan *plan, int32_t heads,
                       int32_t head_dim, float softmax_scale, void *workspace,
                       size_t workspace_bytes, void *dq, void *dk, void *dv, void *stream);
-
-/* Bytes of device workspace mf_attn_bwd_rotated needs: the float32 row dots
- * D and the float32 dQ accumulator (the rotated copies are the forward's). */
-MF_API mf_status mf_attn_bwd_rotated_workspace_size(int32_t total_tokens, int32_t heads,
-                                                    int32_t head_dim, size_t *bytes);
-
-/* mf_attn_bwd from the rotated Q and K that the forward left in its own
- * workspace (mf_attn_fwd or mf_attn_fwd_qkv with the same plan, heads,
- * head_dim and softmax_scale): a training step keeps that workspace from the
- * forward to the backward in place of Q and K.  The gradients are the same
- * as mf_attn_bwd's (review, section "Native-Resolution MMDiT"; dQ and dK are
- * taken with respect to the unrotated inputs), but the backward skips
- * rotating Q and K again and recomputes exactly the forward's fp16 logit
- * operands.
- *   fwd_workspace        device; the forward's workspace, unchanged since that
- *                        call (fp16 q~ = s log2(e) R(q), then k~ = R(k));
- *                        256-byte aligned, >= mf_attn_fwd_workspace_size bytes
- *   workspace            device, >= mf_attn_bwd_rotated_workspace_size bytes,
- *                        256-byte aligned
- *   softmax_scale        the forward's (<= 0 selects 1/sqrt(head_dim) in both)
- * Other arguments, results and errors as mf_attn_bwd (no Q or K arguments). */
-MF_API mf_status mf_attn_bwd_rotated(const void *fwd_workspace, size_t fwd_workspace_bytes,
-                                     const void *v, const void *o, const float *lse,
-                                     const void *dout, const mf_plan *plan, int32_t heads,
-                                     int32_t head_dim, float softmax_scale, void *workspace,
-                                     size_t workspace_bytes, void *dq, void *dk, void *dv,
-                                     void *stream);
 
 /* Size of the fixed device scratch behind mf_attn_bwd_noalloc (128 MiB). */
 #define MF_NOALLOC_SCRATCH_BYTES (128u * 1024u * 1024u)

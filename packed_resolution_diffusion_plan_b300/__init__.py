@@ -17,8 +17,7 @@ import os
 import torch
 
 __all__ = ["MfError", "Plan", "pack_plan", "attn_fwd", "attn_bwd", "check", "record_main_kernel", "lib",
-           "library_path", "fwd_workspace_bytes", "bwd_workspace_bytes", "bwd_rotated_workspace_bytes",
-           "attn_bwd_rotated", "debug_inject", "cfg_combine", "norm_modulate", "gate_residual", "attn_fwd_qkv",
+           "library_path", "fwd_workspace_bytes", "bwd_workspace_bytes", "debug_inject", "cfg_combine", "norm_modulate", "gate_residual", "attn_fwd_qkv",
            "DEBUG_DROP_FWD_KV", "DEBUG_DROP_BWD_QDO", "EXPORTED_SYMBOLS", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,8 +29,7 @@ STATUS = {0: "MF_OK", 1: "MF_ERR_INVALID_ARG", 2: "MF_ERR_UNSUPPORTED", 3: "MF_E
 EXPORTED_SYMBOLS = ["mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd_workspace_size", "mf_attn_fwd",
                     "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_attn_bwd_noalloc", "mf_check",
                     "mf_record_main_kernel", "mf_debug_inject", "mf_cfg_combine", "mf_norm_modulate",
-                    "mf_gate_residual", "mf_attn_fwd_qkv", "mf_attn_bwd_rotated_workspace_size",
-                    "mf_attn_bwd_rotated", "mf_status_string", "mf_last_cuda_error"]
+                    "mf_gate_residual", "mf_attn_fwd_qkv", "mf_status_string", "mf_last_cuda_error"]
 
 TILE = 128
 
@@ -84,9 +82,6 @@ def lib():
     L.mf_attn_bwd_workspace_size.argtypes = [c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]
     L.mf_attn_bwd.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32,
                               ctypes.c_float, c_vp, c_sz, c_vp, c_vp, c_vp, c_vp]
-    L.mf_attn_bwd_rotated_workspace_size.argtypes = [c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)]
-    L.mf_attn_bwd_rotated.argtypes = [c_vp, c_sz, c_vp, c_vp, c_vp, c_vp, ctypes.POINTER(MfPlan), c_i32, c_i32,
-                                      ctypes.c_float, c_vp, c_sz, c_vp, c_vp, c_vp, c_vp]
     L.mf_check.argtypes = [ctypes.POINTER(MfPlan), c_vp]
     L.mf_record_main_kernel.argtypes = [c_vp, c_vp]
     L.mf_debug_inject.argtypes = [c_i32]
@@ -101,8 +96,7 @@ def lib():
     L.mf_last_cuda_error.restype = ctypes.c_char_p
     for name in ("mf_pack_plan_workspace_size", "mf_pack_plan", "mf_attn_fwd_workspace_size", "mf_attn_fwd",
                  "mf_attn_bwd_workspace_size", "mf_attn_bwd", "mf_check", "mf_record_main_kernel",
-                 "mf_debug_inject", "mf_cfg_combine", "mf_norm_modulate", "mf_gate_residual", "mf_attn_fwd_qkv",
-                 "mf_attn_bwd_rotated_workspace_size", "mf_attn_bwd_rotated"):
+                 "mf_debug_inject", "mf_cfg_combine", "mf_norm_modulate", "mf_gate_residual", "mf_attn_fwd_qkv"):
         getattr(L, name).restype = c_i32
     _lib = L
     return L
@@ -273,37 +267,6 @@ def attn_bwd(q, k, v, o, lse, do, plan: Plan, softmax_scale: float = 0.0, worksp
                              ctypes.c_void_p(dq.data_ptr()), ctypes.c_void_p(dk.data_ptr()),
                              ctypes.c_void_p(dv.data_ptr()), _stream_ptr(stream, q.device)),
            "mf_attn_bwd")
-    return dq, dk, dv
-
-
-def bwd_rotated_workspace_bytes(total_tokens: int, heads: int, head_dim: int) -> int:
-    n = ctypes.c_size_t(0)
-    _raise(lib().mf_attn_bwd_rotated_workspace_size(total_tokens, heads, head_dim, ctypes.byref(n)),
-           "mf_attn_bwd_rotated_workspace_size")
-    return n.value
-
-
-def attn_bwd_rotated(fwd_workspace, v, o, lse, do, plan: Plan, softmax_scale: float = 0.0, workspace=None,
-                     dq=None, dk=None, dv=None, stream=None):
-    """dQ, dK, dV from the rotated Q/K the forward left in `fwd_workspace`
-    (see mf_attn_bwd_rotated); softmax_scale must be the forward's."""
-    _check_qkv(plan, v, o, do)
-    T, H, D = v.shape
-    if not (fwd_workspace.is_cuda and fwd_workspace.dtype == torch.uint8 and fwd_workspace.is_contiguous()):
-        raise ValueError("fwd_workspace must be the forward's contiguous uint8 CUDA workspace")
-    if workspace is None:
-        workspace = _workspace(bwd_rotated_workspace_bytes(T, H, D), v.device, stream)
-    dq = torch.empty_like(v) if dq is None else dq
-    dk = torch.empty_like(v) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    _raise(lib().mf_attn_bwd_rotated(ctypes.c_void_p(fwd_workspace.data_ptr()), fwd_workspace.numel(),
-                                     ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(o.data_ptr()),
-                                     ctypes.c_void_p(lse.data_ptr()), ctypes.c_void_p(do.data_ptr()),
-                                     ctypes.byref(plan.raw), H, D, float(softmax_scale),
-                                     ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
-                                     ctypes.c_void_p(dq.data_ptr()), ctypes.c_void_p(dk.data_ptr()),
-                                     ctypes.c_void_p(dv.data_ptr()), _stream_ptr(stream, v.device)),
-           "mf_attn_bwd_rotated")
     return dq, dk, dv
 
 

@@ -310,8 +310,8 @@ mf_status mf_attn_fwd_workspace_size(int32_t total_tokens, int32_t heads, int32_
   if (bytes == nullptr || total_tokens < 0 || heads < 1) return MF_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
   const size_t rows = static_cast<size_t>(total_tokens) * heads;
-  // fp16 q~ | fp16 k~
-  *bytes = 2 * align_up(rows * head_dim * 2, 256);
+  // fp16 k~ | the work counter of the persistent kernel
+  *bytes = align_up(rows * head_dim * 2, 256) + 256;
   return MF_OK;
 }
 
@@ -344,13 +344,14 @@ mf_status attn_fwd_impl(const void* q, const void* k, const void* v, int64_t str
   a.q = q;
   a.k = k;
   a.qk_stride = stride;
-  a.q_rot = ws;
-  a.k_rot = ws + align_up(rows * head_dim * 2, 256);
+  a.k_rot = ws;
+  a.work_counter = reinterpret_cast<int32_t*>(ws + align_up(rows * head_dim * 2, 256));
   a.o = o;
   a.lse = lse;
-  // The main kernel streams the rotated fp16 copies that fwd_pre writes.
+  // The main kernel reads the raw Q rows (rotating them in its prologue) and
+  // streams the rotated fp16 K copy that fwd_pre writes.
   CUtensorMap tq, tk, tv;
-  if ((st = make_tmap(&tq, a.q_rot, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tq, q, plan->total_tokens, heads, head_dim, stride)) != MF_OK) return st;
   if ((st = make_tmap(&tk, a.k_rot, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim, stride)) != MF_OK) return st;
   cudaEvent_t ev0, ev1;
@@ -385,19 +386,9 @@ mf_status mf_attn_bwd_workspace_size(int32_t total_tokens, int32_t heads, int32_
   if (bytes == nullptr || total_tokens < 0 || heads < 1) return MF_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
   const size_t rows = static_cast<size_t>(total_tokens) * heads;
-  // D | float32 dQ accumulator | fp16 q~ | fp16 k~
+  // D | float32 dQ accumulator | fp16 q~ | the work counter of the persistent kernel
   *bytes = align_up(rows * sizeof(float), 256) + align_up(rows * head_dim * sizeof(float), 256) +
-           2 * align_up(rows * head_dim * 2, 256);
-  return MF_OK;
-}
-
-mf_status mf_attn_bwd_rotated_workspace_size(int32_t total_tokens, int32_t heads, int32_t head_dim,
-                                             size_t* bytes) {
-  if (bytes == nullptr || total_tokens < 0 || heads < 1) return MF_ERR_INVALID_ARG;
-  if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
-  const size_t rows = static_cast<size_t>(total_tokens) * heads;
-  // D | float32 dQ accumulator (the rotated copies are the forward's)
-  *bytes = align_up(rows * sizeof(float), 256) + align_up(rows * head_dim * sizeof(float), 256);
+           align_up(rows * head_dim * 2, 256) + 256;
   return MF_OK;
 }
 
@@ -405,70 +396,48 @@ mf_status mf_attn_bwd_rotated_workspace_size(int32_t total_tokens, int32_t heads
 
 namespace {
 
-// The backward from Q and K (fwd_ws == nullptr: bwd_pre writes q~ = R(q) and
-// k~ = s log2(e) R(k) into the workspace) or from the forward's workspace
-// (q~ = s log2(e) R(q), k~ = R(k), left there by mf_attn_fwd / _qkv).
-mf_status attn_bwd_impl(const void* q, const void* k, const void* fwd_ws, size_t fwd_ws_bytes, const void* v,
-                        const void* o, const float* lse, const void* dout, const mf_plan* plan, int32_t heads,
-                        int32_t head_dim, float softmax_scale, void* workspace, size_t workspace_bytes, void* dq,
-                        void* dk, void* dv, void* stream, const char* who) {
+// The backward: bwd_pre writes q~ = s log2(e) R(q) into the workspace beside
+// D and the dQ accumulator; the main kernel rotates each K tile itself.
+mf_status attn_bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, const mf_plan* plan, int32_t heads, int32_t head_dim, float softmax_scale,
+                        void* workspace, size_t workspace_bytes, void* dq, void* dk, void* dv, void* stream,
+                        const char* who) {
   mf_status st = check_attn_common(plan, heads, head_dim);
   if (st != MF_OK) return st;
   if (plan->total_tokens == 0) return MF_OK;
-  const bool from_fwd = fwd_ws != nullptr;
-  if (!from_fwd && (!q || !k)) return MF_ERR_INVALID_ARG;
-  if (!v || !o || !lse || !dout || !workspace || !dq || !dk || !dv) return MF_ERR_INVALID_ARG;
-  if ((!from_fwd && (!aligned16(q) || !aligned16(k))) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+  if (!q || !k || !v || !o || !lse || !dout || !workspace || !dq || !dk || !dv) return MF_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return MF_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MF_ERR_INVALID_ARG;
   size_t need = 0;
-  st = from_fwd ? mf_attn_bwd_rotated_workspace_size(plan->total_tokens, heads, head_dim, &need)
-                : mf_attn_bwd_workspace_size(plan->total_tokens, heads, head_dim, &need);
-  if (st != MF_OK) return st;
+  if ((st = mf_attn_bwd_workspace_size(plan->total_tokens, heads, head_dim, &need)) != MF_OK) return st;
   if (workspace_bytes < need) return MF_ERR_INVALID_ARG;
   const size_t rows = static_cast<size_t>(plan->total_tokens) * heads;
-  const size_t rot_bytes = align_up(rows * head_dim * 2, 256);
-  if (from_fwd) {
-    size_t fwd_need = 0;
-    if ((st = mf_attn_fwd_workspace_size(plan->total_tokens, heads, head_dim, &fwd_need)) != MF_OK) return st;
-    if ((reinterpret_cast<uintptr_t>(fwd_ws) & 255u) != 0 || fwd_ws_bytes < fwd_need) return MF_ERR_INVALID_ARG;
-  }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t off_acc = align_up(rows * sizeof(float), 256);
   const size_t off_qr = off_acc + align_up(rows * head_dim * sizeof(float), 256);
+  const size_t off_ctr = off_qr + align_up(rows * head_dim * 2, 256);
   mf::BwdArgs a;
   a.g = make_geom(plan, heads);
   a.scale = resolve_scale(softmax_scale, head_dim);
   a.scale_log2 = a.scale * kLog2e;
   a.q = q;
-  a.k = k;
   a.o = o;
   a.dout = dout;
   a.lse = lse;
   a.dsum = reinterpret_cast<float*>(ws);
   a.dq_acc = reinterpret_cast<float*>(ws + off_acc);
-  if (from_fwd) {
-    // The forward's copies: q~ carries s log2(e), so dS^T q~ needs ln 2 and
-    // dS k~ needs s.
-    uint8_t* f = static_cast<uint8_t*>(const_cast<void*>(fwd_ws));
-    a.q_rot = f;
-    a.k_rot = f + rot_bytes;
-    a.rotate = 0;
-    a.dk_mult = 1.0f / kLog2e;
-    a.dq_mult = a.scale;
-  } else {
-    a.q_rot = ws + off_qr;
-    a.k_rot = ws + off_qr + rot_bytes;
-    a.rotate = 1;
-    a.dk_mult = a.scale;
-    a.dq_mult = 1.0f / kLog2e;
-  }
-  // The main kernel streams the rotated fp16 copies (16-bit elements: the
-  // tensor maps only move bytes).
+  a.q_rot = ws + off_qr;
+  a.work_counter = reinterpret_cast<int32_t*>(ws + off_ctr);
+  // q~ carries s log2(e): dk~ = s dS^T R(q) = ln 2 (dS^T q~); k~ = R(k): dq~ = s (dS k~)
+  a.dk_mult = 1.0f / kLog2e;
+  a.dq_mult = a.scale;
+  // The main kernel streams the fp16 q~ copy (16-bit elements: the tensor
+  // maps only move bytes) and loads the raw K rows, which it rotates itself.
   CUtensorMap tq, tk, tv, tdo;
   if ((st = make_tmap(&tq, a.q_rot, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
-  if ((st = make_tmap(&tk, a.k_rot, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
+  if ((st = make_tmap(&tk, k, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   if ((st = make_tmap(&tv, v, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   if ((st = make_tmap(&tdo, dout, plan->total_tokens, heads, head_dim)) != MF_OK) return st;
   a.dq = dq;
@@ -491,28 +460,8 @@ mf_status mf_attn_bwd(const void* q, const void* k, const void* v, const void* o
                       const void* dout, const mf_plan* plan, int32_t heads, int32_t head_dim,
                       float softmax_scale, void* workspace, size_t workspace_bytes, void* dq, void* dk,
                       void* dv, void* stream) {
-  if (q == nullptr || k == nullptr) {
-    // an empty pack needs no tensors
-    mf_status st = check_attn_common(plan, heads, head_dim);
-    if (st != MF_OK) return st;
-    return plan->total_tokens == 0 ? MF_OK : MF_ERR_INVALID_ARG;
-  }
-  return attn_bwd_impl(q, k, nullptr, 0, v, o, lse, dout, plan, heads, head_dim, softmax_scale, workspace,
-                       workspace_bytes, dq, dk, dv, stream, "mf_attn_bwd");
-}
-
-mf_status mf_attn_bwd_rotated(const void* fwd_workspace, size_t fwd_workspace_bytes, const void* v, const void* o,
-                              const float* lse, const void* dout, const mf_plan* plan, int32_t heads,
-                              int32_t head_dim, float softmax_scale, void* workspace, size_t workspace_bytes,
-                              void* dq, void* dk, void* dv, void* stream) {
-  if (fwd_workspace == nullptr) {
-    mf_status st = check_attn_common(plan, heads, head_dim);
-    if (st != MF_OK) return st;
-    return plan->total_tokens == 0 ? MF_OK : MF_ERR_INVALID_ARG;
-  }
-  return attn_bwd_impl(nullptr, nullptr, fwd_workspace, fwd_workspace_bytes, v, o, lse, dout, plan, heads,
-                       head_dim, softmax_scale, workspace, workspace_bytes, dq, dk, dv, stream,
-                       "mf_attn_bwd_rotated");
+  return attn_bwd_impl(q, k, v, o, lse, dout, plan, heads, head_dim, softmax_scale, workspace, workspace_bytes, dq,
+                       dk, dv, stream, "mf_attn_bwd");
 }
 
 mf_status mf_check(const mf_plan* plan, void* stream) {

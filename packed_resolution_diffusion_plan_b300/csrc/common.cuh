@@ -78,8 +78,8 @@ struct FwdArgs {
   const void* q;             // bf16, token rows qk_stride elements apart, [heads, D] each
   const void* k;
   int64_t qk_stride;         // heads * D, or 3 heads * D for a QKV projection's rows
-  void* q_rot;               // fp16 [T, heads, D] s log2(e) R(q)
   void* k_rot;               // fp16 [T, heads, D] R(k)
+  int32_t* work_counter;     // the persistent kernel's next work item (zeroed by fwd_pre)
   void* o;                   // bf16 [T, heads, D]
   float* lse;                // [heads, T]
 };
@@ -103,22 +103,17 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUten
 struct BwdArgs {
   AttnGeom g;
   float scale;               // softmax_scale
-  float scale_log2;          // softmax_scale * log2(e)
+  float scale_log2;          // softmax_scale * log2(e), folded into the fp16 q~ copy
   const void* q;             // bf16 [T, heads, D]
-  const void* k;
   const void* o;
   const void* dout;
   const float* lse;
   float* dsum;               // [heads, T] rowsum(dO * O)
-  // fp16 [T, heads, D] rotated copies, one of them scaled by s log2(e):
-  // written by bwd_pre (q~ = R(q), k~ = s log2(e) R(k)) when rotate is set,
-  // else the forward's own (q~ = s log2(e) R(q), k~ = R(k)).
-  void* q_rot;
-  void* k_rot;
-  int rotate;
-  float dk_mult;             // dk~ = dk_mult * (dS^T q~): s, or ln 2 with the forward's copies
-  float dq_mult;             // dq~ = dq_mult * (dS k~): ln 2, or s with the forward's copies
-  float* dq_acc;             // [T, heads, D] float32 accumulator (zeroed by the preprocess)
+  void* q_rot;               // fp16 [T, heads, D] q~ = s log2(e) R(q), written by bwd_pre
+  float dk_mult;             // dk~ = dk_mult * (dS^T q~) = ln 2 * (dS^T q~)
+  float dq_mult;             // dq~ = dq_mult * (dS k~) = s * (dS k~), k~ = R(k) unscaled
+  float* dq_acc;             // [T, heads, D] float32 accumulator (zeroed by bwd_pre)
+  int32_t* work_counter;     // the persistent kernel's next work item (zeroed by bwd_pre)
   void* dq;
   void* dk;
   void* dv;

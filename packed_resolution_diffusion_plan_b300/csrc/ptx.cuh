@@ -265,6 +265,49 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The two 32-bit halves of an sdesc<kLbo, kSbo> descriptor.  An MMA issue
+// loop keeps one low half per operand tile and adds each MMA's offset
+// (>> 4) to it, so that the issuing thread neither holds every MMA's
+// 64-bit descriptor in registers nor redoes the whole encoding per MMA.
+template <uint32_t kLbo>
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr) {
+  return ((saddr >> 4) & 0x3FFFu) | (((kLbo >> 4) & 0x3FFFu) << 16);
+}
+template <uint32_t kSbo>
+__host__ __device__ constexpr uint32_t sdesc_hi() {
+  return ((kSbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+// A 32-bit value the compiler must recompute where it is used (no hoisting
+// out of loops): keeps per-MMA descriptor arithmetic next to the MMA.
+__device__ __forceinline__ uint32_t opaque_u32(uint32_t x) {
+  uint32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+// mma_ss / mma_ts with the shared-memory descriptors given as (low half,
+// shared high half).
+__device__ __forceinline__ void mma_ss_lh(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 da, {%1, %3};\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_lh(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(hi)
+      : "memory");
+}
+
 // Register rebalancing between warpgroups: every warp of a warpgroup runs the
 // same setmaxnreg; the shares of all warpgroups must add up to no more than
 // the registers the CTA was launched with.

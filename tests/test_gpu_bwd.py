@@ -13,9 +13,7 @@ from _parity import assert_close, lse_tol_factor, to64
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_fwd_bwd(samples, heads, head_dim, seed, budget=0, scale=0.0, rotated=False):
-    """rotated: the backward reads the rotated Q/K copies the forward left in
-    its workspace (mf_attn_bwd_rotated) instead of rotating Q and K again."""
+def _gpu_fwd_bwd(samples, heads, head_dim, seed, budget=0, scale=0.0):
     wl = synth.Workload("t", samples, heads, head_dim, "fwd+bwd", token_budget=budget, seed=seed)
     t = synth.draw_tensors(wl, with_grad=True)
     plan = mf.pack_plan(samples, token_budget=budget, head_dim=head_dim)
@@ -23,16 +21,13 @@ def _gpu_fwd_bwd(samples, heads, head_dim, seed, budget=0, scale=0.0, rotated=Fa
     q, k, v, do = (t[n][:T].cuda() for n in ("q", "k", "v", "do"))
     wsf = torch.empty(max(256, mf.fwd_workspace_bytes(T, heads, head_dim)), dtype=torch.uint8, device="cuda")
     o, lse = mf.attn_fwd(q, k, v, plan, softmax_scale=scale, workspace=wsf)
-    if rotated:
-        dq, dk, dv = mf.attn_bwd_rotated(wsf, v, o, lse, do, plan, softmax_scale=scale)
-    else:
-        dq, dk, dv = mf.attn_bwd(q, k, v, o, lse, do, plan, softmax_scale=scale)
+    dq, dk, dv = mf.attn_bwd(q, k, v, o, lse, do, plan, softmax_scale=scale)
     mf.check(plan)
     return plan, (q, k, v, do), (dq, dk, dv)
 
 
-def _run_full(samples, heads, head_dim, seed, budget=0, scale=0.0, rotated=False):
-    plan, (q, k, v, do), (dq, dk, dv) = _gpu_fwd_bwd(samples, heads, head_dim, seed, budget, scale, rotated)
+def _run_full(samples, heads, head_dim, seed, budget=0, scale=0.0):
+    plan, (q, k, v, do), (dq, dk, dv) = _gpu_fwd_bwd(samples, heads, head_dim, seed, budget, scale)
     ref = oracle.pack_plan(samples, budget)
     cu, pos = ref["cu_seqlens"], ref["pos"]
     qn, kn, vn, gn = to64(q), to64(k), to64(v), to64(do)
@@ -44,34 +39,30 @@ def _run_full(samples, heads, head_dim, seed, budget=0, scale=0.0, rotated=False
     assert_close("dQ", to64(dq), rq, "grad", f)
 
 
-@pytest.mark.parametrize("rotated", [False, True])
 @pytest.mark.parametrize("seed", range(3))
-def test_bwd_tiny(seed, rotated):
+def test_bwd_tiny(seed):
     wl = synth.tiny(seed)
-    _run_full(wl.samples, wl.heads, wl.head_dim, seed, rotated=rotated)
+    _run_full(wl.samples, wl.heads, wl.head_dim, seed)
 
 
-@pytest.mark.parametrize("rotated", [False, True])
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("seed", range(2))
-def test_bwd_ragged_multi_tile(head_dim, seed, rotated):
+def test_bwd_ragged_multi_tile(head_dim, seed):
     samples = [(0, 16, 16), (7, 64, 32), (0, 128, 128), (200, 160, 48), (1, 16, 16), (55, 96, 208)]
     rng = np.random.default_rng(seed)
     rng.shuffle(samples)
-    _run_full(samples, heads=3, head_dim=head_dim, seed=seed, rotated=rotated)
+    _run_full(samples, heads=3, head_dim=head_dim, seed=seed)
 
 
-@pytest.mark.parametrize("rotated", [False, True])
 @pytest.mark.parametrize("L", [1, 127, 128, 129, 256, 300])
-def test_bwd_tile_boundaries(L, rotated):
-    _run_full([(0, 16, 16 * L)], heads=2, head_dim=128, seed=L, rotated=rotated)
+def test_bwd_tile_boundaries(L):
+    _run_full([(0, 16, 16 * L)], heads=2, head_dim=128, seed=L)
 
 
-@pytest.mark.parametrize("rotated", [False, True])
 @pytest.mark.parametrize("head_dim", [64, 128])
-def test_bwd_text_only_and_image_only_samples(head_dim, rotated):
+def test_bwd_text_only_and_image_only_samples(head_dim):
     _run_full([(40, 0, 0), (0, 48, 48), (1, 0, 0), (129, 0, 0), (3, 32, 32), (0, 16, 16 * 127)],
-              heads=2, head_dim=head_dim, seed=head_dim, rotated=rotated)
+              heads=2, head_dim=head_dim, seed=head_dim)
 
 
 def test_bwd_single_token_closed_form():
@@ -81,28 +72,15 @@ def test_bwd_single_token_closed_form():
     assert torch.equal(dv[0], do[0])
 
 
-@pytest.mark.parametrize("rotated", [False, True])
-def test_bwd_budget_prefix(rotated):
-    _run_full([(30, 96, 96), (12, 64, 48), (0, 48, 160)], heads=2, head_dim=64, seed=6, budget=80, rotated=rotated)
+def test_bwd_budget_prefix():
+    _run_full([(30, 96, 96), (12, 64, 48), (0, 48, 160)], heads=2, head_dim=64, seed=6, budget=80)
 
 
-@pytest.mark.parametrize("rotated", [False, True])
 @pytest.mark.parametrize("scale", [0.05, 0.3])
-def test_bwd_explicit_softmax_scale(scale, rotated):
-    """A scale other than 1/sqrt(d): the two backward entry points put it on
-    different operands and multiply dK and dQ back differently."""
-    _run_full([(9, 64, 96), (0, 160, 32), (33, 0, 0)], heads=2, head_dim=128, seed=11, scale=scale, rotated=rotated)
-
-
-def test_bwd_rotated_close_to_plain():
-    """Both entry points compute the same gradients; they differ only in which
-    fp16 operand carries the s log2(e) factor."""
-    samples = [(20, 96, 128), (0, 64, 64), (5, 32, 208)]
-    _, _, g0 = _gpu_fwd_bwd(samples, 3, 128, 4)
-    _, _, g1 = _gpu_fwd_bwd(samples, 3, 128, 4, rotated=True)
-    for a, b in zip(g0, g1):
-        a, b = a.double(), b.double()
-        assert float((a - b).norm() / b.norm()) < 5e-3
+def test_bwd_explicit_softmax_scale(scale):
+    """A scale other than 1/sqrt(d), carried by one fp16 logit operand and
+    multiplied back out of dK and dQ."""
+    _run_full([(9, 64, 96), (0, 160, 32), (33, 0, 0)], heads=2, head_dim=128, seed=11, scale=scale)
 
 
 def test_bwd_empty_pack():
@@ -113,23 +91,16 @@ def test_bwd_empty_pack():
     dq, dk, dv = mf.attn_bwd(z, z, z, z, lse, z, plan_d)
     mf.check(plan_d)
     assert dq.shape == (0, 2, 64)
-    wsf = torch.empty(256, dtype=torch.uint8, device="cuda")
-    dq, dk, dv = mf.attn_bwd_rotated(wsf, z, z, lse, z, plan_d)
-    mf.check(plan_d)
-    assert dk.shape == (0, 2, 64)
 
 
-@pytest.mark.parametrize("name,samples_idx,rotated", [("native_res_32k", [2, 5], True),
-                                                     ("native_res_32k", [2], False),
-                                                     ("extreme_aspect", [0], True)])
-def test_bwd_full_size_per_sample(name, samples_idx, rotated):
-    """Full-size pack in the bench's launch configuration (the backward from the
-    forward's rotated copies); the oracle recomputes selected samples on a few
-    heads (samples are independent, so a sample's gradients depend only on its
-    own rows)."""
+@pytest.mark.parametrize("name,samples_idx", [("native_res_32k", [2, 5]), ("extreme_aspect", [0])])
+def test_bwd_full_size_per_sample(name, samples_idx):
+    """Full-size pack in the bench's launch configuration; the oracle
+    recomputes selected samples on a few heads (samples are independent, so a
+    sample's gradients depend only on its own rows)."""
     wl = synth.WORKLOADS[name]()
     plan, (q, k, v, do), (dq, dk, dv) = _gpu_fwd_bwd(wl.samples, wl.heads, wl.head_dim, wl.seed,
-                                                     wl.token_budget, rotated=rotated)
+                                                     wl.token_budget)
     ref = oracle.pack_plan(wl.samples, wl.token_budget)
     cu = ref["cu_seqlens"]
     dq_c, dk_c, dv_c = to64(dq), to64(dk), to64(dv)
@@ -162,9 +133,9 @@ def test_bwd_full_size_long_samples_rows(name, samples_idx):
     """The long samples that dominate the benched fwd+bwd packs (10,749 and
     10,577 tokens of the training pack, 16,640 of the extreme-aspect pack: up
     to 130 K/V tiles whose dQ partials meet in one accumulator row), in the
-    bench's launch configuration, through both backward entry points, on every
-    head: sampled query rows (dQ) and key rows (dK, dV) against the row-wise
-    oracle, which takes each sample's full-row statistics."""
+    bench's launch configuration, on every head: sampled query rows (dQ) and
+    key rows (dK, dV) against the row-wise oracle, which takes each sample's
+    full-row statistics."""
     wl = synth.WORKLOADS[name]()
     t = synth.draw_tensors(wl, with_grad=True)
     plan = mf.pack_plan(wl.samples, token_budget=wl.token_budget, head_dim=wl.head_dim)
@@ -172,8 +143,7 @@ def test_bwd_full_size_long_samples_rows(name, samples_idx):
     q, k, v, do = (t[n][:T].cuda() for n in ("q", "k", "v", "do"))
     wsf = torch.empty(mf.fwd_workspace_bytes(T, wl.heads, wl.head_dim), dtype=torch.uint8, device="cuda")
     o, lse = mf.attn_fwd(q, k, v, plan, workspace=wsf)
-    got = {"rotated": mf.attn_bwd_rotated(wsf, v, o, lse, do, plan),
-           "plain": mf.attn_bwd(q, k, v, o, lse, do, plan)}
+    got = {"bwd": mf.attn_bwd(q, k, v, o, lse, do, plan)}
     mf.check(plan)
     got = {e: [to64(x) for x in g] for e, g in got.items()}
     for g in got.values():
@@ -193,3 +163,38 @@ def test_bwd_full_size_long_samples_rows(name, samples_idx):
             assert_close(f"dQ[{name},{e},h{h}]", dq[q_rows, h], rq, "grad")
             assert_close(f"dK[{name},{e},h{h}]", dk[kv_rows, h], rk, "grad")
             assert_close(f"dV[{name},{e},h{h}]", dv[kv_rows, h], rv, "grad")
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_bwd_non_finite_values_stay_in_their_sample(head_dim):
+    """NaN and Inf in one sample's V and dO (and NaN in its Q and K) leave
+    every other sample's dQ, dK, dV as without them.  Tiles that run past a
+    sample's end read the next sample's rows: a zero P or dS times a
+    non-finite q~, dO or k~ value would otherwise be NaN, and dQ rows past a
+    sample's end are reduced into the next sample's rows."""
+    samples = [(5, 256, 208), (3, 160, 160), (0, 16, 16 * 77), (9, 64, 16 * 30)]
+    heads = 2
+    wl = synth.Workload("t", samples, heads, head_dim, "fwd+bwd", seed=43)
+    t = synth.draw_tensors(wl, with_grad=True)
+    ref = oracle.pack_plan(samples)
+    cu = ref["cu_seqlens"]
+    a, b = int(cu[1]), int(cu[2])
+    q, k, v, do = (t[n].clone() for n in ("q", "k", "v", "do"))
+    v[a:b, 0] = float("nan")
+    v[a:b, 1] = float("inf")
+    do[a:b, 0] = float("-inf")
+    do[a + 2:b, 1, 9:] = float("nan")
+    q[a + 1:b, :, :5] = float("nan")
+    k[a:b - 2, :, 3:9] = float("nan")
+    plan = mf.pack_plan(samples, head_dim=head_dim)
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    o, lse = mf.attn_fwd(qd, kd, vd, plan)
+    dq, dk, dv = mf.attn_bwd(qd, kd, vd, o, lse, dod, plan)
+    mf.check(plan)
+    qn, kn, vn, gn = (to64(t[n]) for n in ("q", "k", "v", "do"))
+    O, L = oracle.attn_fwd(qn, kn, vn, cu, ref["pos"])
+    rq, rk, rv = oracle.attn_bwd(qn, kn, vn, O, L, gn, cu, ref["pos"])
+    keep = np.r_[0:a, b:int(cu[-1])]
+    assert_close("dV outside the poisoned sample", to64(dv)[keep], rv[keep], "grad")
+    assert_close("dK outside the poisoned sample", to64(dk)[keep], rk[keep], "grad")
+    assert_close("dQ outside the poisoned sample", to64(dq)[keep], rq[keep], "grad")

@@ -72,9 +72,9 @@ def test_attn_fwd_qkv_equals_split_tensors(head_dim, heads):
 
 
 @pytest.mark.parametrize("rope_axes", [2, 3])
-def test_bwd_rotated_from_qkv_forward(rope_axes):
-    """The backward from the rotated copies that the QKV-row forward leaves in
-    its workspace, against the oracle's gradients."""
+def test_bwd_after_qkv_forward(rope_axes):
+    """The backward of the QKV-row forward (its O and LSE, the projection's
+    thirds as Q, K, V), against the oracle's gradients."""
     heads, head_dim = 4, 128
     samples = synth.random_pack(700 + rope_axes, 4, 70, 12, edit=rope_axes == 3)
     plan = mf.pack_plan(samples, head_dim=head_dim, rope_axes=rope_axes)
@@ -84,10 +84,9 @@ def test_bwd_rotated_from_qkv_forward(rope_axes):
     do = _bf16(g, T, heads, head_dim)
     wsf = torch.empty(max(256, mf.fwd_workspace_bytes(T, heads, head_dim)), dtype=torch.uint8, device="cuda")
     o, lse = mf.attn_fwd_qkv(qkv, plan, heads, workspace=wsf)
-    v = qkv[:, 2 * C:].contiguous().view(T, heads, head_dim)
-    dq, dk, dv = mf.attn_bwd_rotated(wsf, v, o, lse, do, plan)
+    q, k, v = (qkv[:, i * C:(i + 1) * C].contiguous().view(T, heads, head_dim) for i in range(3))
+    dq, dk, dv = mf.attn_bwd(q, k, v, o, lse, do, plan)
     mf.check(plan)
-    q, k = (qkv[:, i * C:(i + 1) * C].contiguous().view(T, heads, head_dim) for i in range(2))
     ref = oracle.pack_plan(samples)
     rope = dict(frame=ref["frame"], rope_axes=rope_axes)
     qn, kn, vn = to64(q), to64(k), to64(v)

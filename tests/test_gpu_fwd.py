@@ -129,3 +129,32 @@ def test_fwd_range_report_and_clear():
     k[3, 1, 5] = 1.0
     mf.attn_fwd(q, k, v, plan)
     mf.check(plan)
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_fwd_non_finite_values_stay_in_their_sample(head_dim):
+    """NaN and Inf in one sample's V (and NaN in its Q and K) leave every
+    other sample's O and LSE exactly as without them: tiles that run past a
+    sample's end read the next sample's rows, and a masked logit (P = 0)
+    times a non-finite V value would otherwise be NaN.  The neighbours'
+    lengths are ragged, so their last tiles reach into the poisoned sample."""
+    samples = [(5, 256, 208), (3, 160, 160), (0, 16, 16 * 77), (9, 64, 16 * 30)]
+    heads = 2
+    wl = synth.Workload("t", samples, heads, head_dim, "fwd", seed=41)
+    t = synth.draw_tensors(wl, with_grad=False)
+    ref = oracle.pack_plan(samples)
+    cu = ref["cu_seqlens"]
+    a, b = int(cu[1]), int(cu[2])
+    q, k, v = (t[n].clone() for n in ("q", "k", "v"))
+    v[a:b, 0] = float("nan")
+    v[a:b, 1] = float("inf")
+    v[a + 3, 1, 7] = float("-inf")
+    q[a + 1:b, :, :5] = float("nan")
+    k[a:b - 2, :, 3:9] = float("nan")
+    plan = mf.pack_plan(samples, head_dim=head_dim)
+    o, lse = mf.attn_fwd(q.cuda(), k.cuda(), v.cuda(), plan)
+    mf.check(plan)
+    O, L = oracle.attn_fwd(to64(t["q"]), to64(t["k"]), to64(t["v"]), cu, ref["pos"])
+    keep = np.r_[0:a, b:int(cu[-1])]
+    assert_close("O outside the poisoned sample", to64(o)[keep], O[keep], "o")
+    assert_close("LSE outside the poisoned sample", to64(lse)[:, keep], L[:, keep], "lse")

@@ -30,7 +30,10 @@ def _inputs():
 
 def _expect_timeout(plan, kernel, n_ctas):
     """MF_ERR_TIMEOUT, with the record naming the kernel, a barrier of its
-    barrier block and every CTA (each one's loads were dropped)."""
+    barrier block and between one and n_ctas CTAs: every CTA of the
+    persistent kernel that took a work item gives up, and with the loads
+    dropped a CTA may take a second item before its first wait runs out,
+    leaving others none."""
     t0 = time.time()
     with pytest.raises(mf.MfError) as ei:
         mf.check(plan)
@@ -40,7 +43,7 @@ def _expect_timeout(plan, kernel, n_ctas):
     assert m, str(ei.value)
     assert m.group(1) == kernel
     assert int(m.group(2)) < 32
-    assert int(m.group(3)) == n_ctas
+    assert 1 <= int(m.group(3)) <= n_ctas
     mf.check(plan)  # the status word and the record were cleared
 
 
@@ -51,7 +54,7 @@ def test_fwd_dropped_loads_time_out_then_recover():
         mf.attn_fwd(q, k, v, plan)
     finally:
         mf.debug_inject(0)
-    _expect_timeout(plan, "attn_fwd_kernel", plan.n_pairs * q.shape[1])
+    _expect_timeout(plan, "attn_fwd_kernel", min(plan.n_pairs * q.shape[1], torch.cuda.get_device_properties(0).multi_processor_count))
     o, lse = mf.attn_fwd(q, k, v, plan)
     mf.check(plan)
     ref = oracle.pack_plan(wl.samples)
@@ -69,7 +72,7 @@ def test_bwd_dropped_loads_time_out_then_recover():
         mf.attn_bwd(q, k, v, o, lse, do, plan)
     finally:
         mf.debug_inject(0)
-    _expect_timeout(plan, "bwd_main_kernel", plan.n_tiles * q.shape[1])
+    _expect_timeout(plan, "bwd_main_kernel", min(plan.n_tiles * q.shape[1], torch.cuda.get_device_properties(0).multi_processor_count))
     dq, dk, dv = mf.attn_bwd(q, k, v, o, lse, do, plan)
     mf.check(plan)
     ref = oracle.pack_plan(wl.samples)
