@@ -74,7 +74,7 @@ constexpr int kRowWarp = 11;
 constexpr float kLog2e = 1.4426950408889634f;
 // Per-thread register shares after setmaxnreg; they add up to the launch's
 // 3 x 168 per thread (65,536 / 384 rounded down to a multiple of 8).
-constexpr uint32_t kRegsCompute = 208, kRegsCtrl = 88;
+constexpr uint32_t kRegsCompute = 216, kRegsCtrl = 72;
 static_assert(2 * kRegsCompute + kRegsCtrl <= 3 * 168, "warpgroup register shares exceed the launch's registers");
 
 // Barriers and CTA-wide scalars of bwd_main, kept in dynamic shared memory
