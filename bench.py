@@ -726,7 +726,9 @@ def run_chain(args):
             "chain_ms": {"fused": round(f_chain, 4), "unfused": round(u_chain, 4)},
             "block_ms": {"fused": round(f_block, 4), "unfused": round(u_block, 4)},
             "block_speedup": u_block / f_block,
-            "chain_hbm_gbs_fused": (2 * T * C * 2 + (2 * T * C * 2 + 2 * T * C * 2) + 3 * T * C * 2) / (f_chain * 1e-3) / 1e9,
+            # x read, y written; k read, k~ written (q is rotated from the QKV rows
+            # inside the attention kernel); x, z read, out written
+            "chain_hbm_gbs_fused": (2 * T * C * 2 + 2 * T * C * 2 + 3 * T * C * 2) / (f_chain * 1e-3) / 1e9,
             "clocks": clk}
     print(json.dumps(line), flush=True)
     return 0
