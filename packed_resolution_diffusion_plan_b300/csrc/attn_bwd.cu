@@ -82,16 +82,20 @@ static_assert(2 * kRegsCompute + kRegsCtrl <= 3 * 168, "warpgroup register share
 // base is the start of the CTA's window and the tiles stay 1024-aligned).
 // A timeout record names a barrier by its position here: kv_full 0, kv_ready
 // 1, kv_empty 2, acc_full 3, fin 4, item_full 5-6, item_empty 7-8, q_full
-// 9-10, q_ready 11-12, q_free 13-14, do_full 15, do_free 16, q_tail 17,
-// do_tail 18, tail_fixed 19, s_full 20, p_ready 21, dp_full 22, ds_ready 23,
-// a_free 24, dq_full 25, dq_free 26, stage_full 27-28, stage_free 29,
-// q_issued 30.
+// 9-10, q_ready 11-12, q_free 13-14, do_full 15, do_free 16, q_tail 17-18,
+// do_tail 19-20, tail_fixed 21-22, s_full 23, p_ready 24, dp_full 25,
+// ds_ready 26, a_free 27, dq_full 28, dq_free 29, stage_full 30-31,
+// stage_free 32, q_issued 33.
 // The last Q tile of an item whose sample ends inside it (a "ragged" item)
 // lands on q_tail / do_tail instead of its slots' q_full / do_full (whose
 // phases the producer completes with plain arrivals, so that they stay in
 // step); the row warp zeroes its rows past the end and arrives on
-// tail_fixed, which the MMA issuer waits for instead.
-constexpr uint32_t kBwdBarriers = 31;
+// tail_fixed, which the MMA issuer waits for instead.  Ragged item n uses
+// the tail barriers n % 2: with one set, two short ragged items in a row
+// could complete two phases of a tail barrier before its waiter looked (the
+// next tail needs only the other q~ slot), and a parity wait would then
+// take the later phase for the one it wants.
+constexpr uint32_t kBwdBarriers = 34;
 constexpr uint32_t kTimeoutKernelBwd = 2;
 // Arrivals on an item slot's "read" barrier: the MMA and reducer threads, the
 // row warp and the eight compute warps (one per warp).
@@ -100,7 +104,7 @@ struct BwdCtl {
   uint64_t kv_full, kv_ready, kv_empty, acc_full, fin;
   uint64_t item_full[2], item_empty[2];
   uint64_t q_full[2], q_ready[2], q_free[2], do_full, do_free;
-  uint64_t q_tail, do_tail, tail_fixed;
+  uint64_t q_tail[2], do_tail[2], tail_fixed[2];
   uint64_t s_full, p_ready, dp_full, ds_ready, a_free, dq_full, dq_free;
   uint64_t stage_full[2], stage_free, q_issued;
   uint32_t tmem;
@@ -313,9 +317,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     }
     mbar_init(&c.do_full, 1);
     mbar_init(&c.do_free, 1);
-    mbar_init(&c.q_tail, 1);
-    mbar_init(&c.do_tail, 1);
-    mbar_init(&c.tail_fixed, 32);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&c.q_tail[s], 1);
+      mbar_init(&c.do_tail[s], 1);
+      mbar_init(&c.tail_fixed[s], 32);
+    }
     mbar_init(&c.s_full, 1);
     mbar_init(&c.p_ready, 2 * kTile);
     mbar_init(&c.dp_full, 1);
@@ -389,7 +395,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           uint64_t* bar = &c.q_full[s];
           if (ragged && i == n_q - 1) {
             mbar_arrive(bar);          // the slot's phase, without the data
-            bar = &c.q_tail;
+            bar = &c.q_tail[tail_loads & 1];
           }
           q_loads = g + 1;
           mbar_arrive_expect_tx(bar, C::kTileBytes);
@@ -406,7 +412,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           uint64_t* bar = &c.do_full;
           if (ragged && i == n_q - 1) {
             mbar_arrive(bar);
-            bar = &c.do_tail;
+            bar = &c.do_tail[tail_loads & 1];
             ++tail_loads;
           }
           do_loads = g + 1;
@@ -440,9 +446,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       if (kv_loads) wait_drain(&c.kv_full, (kv_loads - 1) & 1, abort_flag);
       for (int g = q_loads > 2 ? q_loads - 2 : 0; g < q_loads; ++g) wait_drain(&c.q_full[g & 1], (g >> 1) & 1, abort_flag);
       if (do_loads) wait_drain(&c.do_full, (do_loads - 1) & 1, abort_flag);
-      if (tail_loads) {
-        wait_drain(&c.q_tail, (tail_loads - 1) & 1, abort_flag);
-        wait_drain(&c.do_tail, (tail_loads - 1) & 1, abort_flag);
+      for (int t = tail_loads > 2 ? tail_loads - 2 : 0; t < tail_loads; ++t) {
+        wait_drain(&c.q_tail[t & 1], (t >> 1) & 1, abort_flag);
+        wait_drain(&c.do_tail[t & 1], (t >> 1) & 1, abort_flag);
       }
     } else if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t id_st = idesc_f16(kTile, kTile, false, false);   // k~ q~^T
@@ -490,7 +496,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // tail_fixed (after the tail's rows past the sample's end are zeroed).
         auto q_in = [&](int i) -> bool {
           const int g = gq + i;
-          if (ragged && i == n_q - 1) return mbar_wait(&c.tail_fixed, n_tail & 1, abort_flag);
+          if (ragged && i == n_q - 1) return mbar_wait(&c.tail_fixed[n_tail & 1], (n_tail >> 1) & 1, abort_flag);
           return mbar_wait(&c.q_full[g & 1], (g >> 1) & 1, abort_flag);
         };
         auto do_in = [&](int i) -> bool {
@@ -637,7 +643,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           mbar_arrive(&c.q_ready[s]);
           if (valid_rows < kTile) {
             // the ragged item's last tile (only the last can be short)
-            if (!warp_wait(&c.q_tail, n_tail & 1, abort_flag) || !warp_wait(&c.do_tail, n_tail & 1, abort_flag)) {
+            if (!warp_wait(&c.q_tail[n_tail & 1], (n_tail >> 1) & 1, abort_flag) ||
+                !warp_wait(&c.do_tail[n_tail & 1], (n_tail >> 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
@@ -651,7 +658,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
               *reinterpret_cast<uint4*>(dt + off) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
-            mbar_arrive(&c.tail_fixed);
+            mbar_arrive(&c.tail_fixed[n_tail & 1]);
             ++n_tail;
           }
         }

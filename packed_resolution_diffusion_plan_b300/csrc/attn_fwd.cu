@@ -128,18 +128,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   uint8_t* smem = align1024(smem_raw);
   // One block of barriers, so that a timeout record can name one by its
   // position: final 0, item_full 1-2, item_empty 3-4, q_full 5-6, q_ready
-  // 7-8, q_empty 9-10, v_tail 11, v_fixed 12, k_full 13.., k_free, v_full,
-  // v_free, s_full, p_full, pv_done (two each for the last three).
+  // 7-8, q_empty 9-10, v_tail 11-12, v_fixed 13-14, k_full 15.., k_free,
+  // v_full, v_free, s_full, p_full, pv_done (two each for the last three).
   // The last V tile of an item whose sample ends inside it (a "ragged" item)
   // lands on v_tail instead of its slot's v_full (whose phase the producer
   // completes with a plain arrival, so that the slot's phases stay in step):
   // the prep warps wait for that tile on v_tail, zero its rows past the
   // sample's end and arrive on v_fixed, which the MMA waits for instead.
+  // Ragged item n uses v_tail / v_fixed n % 2: with one of each, two short
+  // ragged items in a row could complete two phases before a waiter looked
+  // (the next tail needs only the other V slot), and a parity wait would
+  // then take the later phase for the one it wants.
   struct Bars {
     uint64_t final;
     uint64_t item_full[2], item_empty[2];
     uint64_t q_full[2], q_ready[2], q_empty[2];
-    uint64_t v_tail, v_fixed;
+    uint64_t v_tail[2], v_fixed[2];
     uint64_t k_full[C::kKStages], k_free[C::kKStages];
     uint64_t v_full[C::kVStages], v_free[C::kVStages];
     uint64_t s_full[2], p_full[2], pv_done[2];
@@ -162,8 +166,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       mbar_init(&bars.p_full[i], kTile);
       mbar_init(&bars.pv_done[i], 1);
     }
-    mbar_init(&bars.v_tail, 1);
-    mbar_init(&bars.v_fixed, kPrepThreads);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.v_tail[i], 1);
+      mbar_init(&bars.v_fixed[i], kPrepThreads);
+    }
     for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&bars.k_full[i], 1);
       mbar_init(&bars.k_free[i], 1);
@@ -257,7 +263,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           uint64_t* bar = &bars.v_full[s];
           if (ragged && j == n_kv - 1) {
             mbar_arrive(bar);           // the slot's phase, without the data
-            bar = &bars.v_tail;
+            bar = &bars.v_tail[tail_issued & 1];
             ++tail_issued;
           }
           mbar_arrive_expect_tx(bar, C::kTileBytes);
@@ -288,7 +294,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         wait_drain(&bars.k_full[g % C::kKStages], (g / C::kKStages) & 1, abort_flag);
       for (long long g = v_issued > C::kVStages ? v_issued - C::kVStages : 0; g < v_issued; ++g)
         wait_drain(&bars.v_full[g % C::kVStages], (g / C::kVStages) & 1, abort_flag);
-      if (tail_issued > 0) wait_drain(&bars.v_tail, (tail_issued - 1) & 1, abort_flag);
+      for (int t = tail_issued > 2 ? tail_issued - 2 : 0; t < tail_issued; ++t)
+        wait_drain(&bars.v_tail[t & 1], (t >> 1) & 1, abort_flag);
     } else if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(kTile, kTile, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(kTile, D, false, true);
@@ -328,7 +335,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // too: the previous item's last PV_a).
         auto v_ready = [&](int j) -> bool {
           const long long g = gs + j;
-          if (ragged && j == n_kv - 1) return mbar_wait(&bars.v_fixed, n_ragged & 1, abort_flag);
+          if (ragged && j == n_kv - 1) return mbar_wait(&bars.v_fixed[n_ragged & 1], (n_ragged >> 1) & 1, abort_flag);
           return mbar_wait(&bars.v_full[g % C::kVStages], (g / C::kVStages) & 1, abort_flag);
         };
         ok = mbar_wait(&bars.q_ready[0], k & 1, abort_flag) &&
@@ -401,7 +408,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           // Zero the last V tile's rows past the sample's end (their P is 0,
           // but 0 times a non-finite value is not).
           const long long g = vc + n_kv - 1;
-          if (!warp_wait(&bars.v_tail, n_ragged & 1, abort_flag)) break;
+          if (!warp_wait(&bars.v_tail[n_ragged & 1], (n_ragged >> 1) & 1, abort_flag)) break;
           uint8_t* vt = smem + C::kOffV + static_cast<int>(g % C::kVStages) * C::kTileBytes;
           for (int c = t; c < (kTile - last_valid) * 8 * C::kHalves; c += kPrepThreads) {
             const int r = last_valid + c / (8 * C::kHalves);
@@ -410,7 +417,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
-          mbar_arrive(&bars.v_fixed);
+          mbar_arrive(&bars.v_fixed[n_ragged & 1]);
           ++n_ragged;
         }
         vc += n_kv;

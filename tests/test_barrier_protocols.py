@@ -88,12 +88,15 @@ class Barrier:
 # rows past the end before the MMAs read them).
 # --------------------------------------------------------------------------
 
-def _bwd_roles(items, fixed, head_dim=128, tail_bars=True):
+def _bwd_roles(items, fixed, head_dim=128, tail_bars=True, tail_slots=2):
     """head_dim 64 has no reducer: dQ leaves by atomics, q_free takes the
-    MMA's arrival alone and staging is a no-op.  fixed=False restores the
-    staging protocol before warpgroup 1 waited for the reducer;
+    MMA's arrival alone and staging is a no-op.  Ragged item n uses the tail
+    barriers q_tail / do_tail / tail_fixed n % tail_slots.  fixed=False
+    restores the staging protocol before warpgroup 1 waited for the reducer;
     tail_bars=False has the row warp wait for a ragged tile on its slots'
-    q_full / do_full, skipping their earlier phases (checks of the checker)."""
+    q_full / do_full, skipping their earlier phases; tail_slots=1 shares one
+    set of tail barriers among all ragged items (checks of the checker)."""
+    T = tail_slots
     a_all = ["A0P", "A0S", "A1P", "A1S"]
     n_items = len(items)
 
@@ -120,7 +123,7 @@ def _bwd_roles(items, fixed, head_dim=128, tail_bars=True):
                     yield ("wait", f"q_free{s}", (g >> 1) - 1)
                 if ragged and i == n_q - 1 and tail_bars:
                     yield ("arrive", f"q_full{s}")
-                    yield ("tma", "q_tail", [f"Q{s}"])
+                    yield ("tma", f"q_tail{n_tail % T}", [f"Q{s}"])
                 else:
                     yield ("tma", f"q_full{s}", [f"Q{s}"])
 
@@ -130,7 +133,7 @@ def _bwd_roles(items, fixed, head_dim=128, tail_bars=True):
                     yield ("wait", "do_free", g - 1)
                 if ragged and i == n_q - 1 and tail_bars:
                     yield ("arrive", "do_full")
-                    yield ("tma", "do_tail", ["DO"])
+                    yield ("tma", f"do_tail{n_tail % T}", ["DO"])
                 else:
                     yield ("tma", "do_full", ["DO"])
 
@@ -153,9 +156,10 @@ def _bwd_roles(items, fixed, head_dim=128, tail_bars=True):
             for g in range(max(0, gq - 2), gq):
                 yield ("wait", f"q_full{g & 1}", g >> 1)
             yield ("wait", "do_full", gq - 1)
-        if n_tail and tail_bars:
-            yield ("wait", "q_tail", n_tail - 1)
-            yield ("wait", "do_tail", n_tail - 1)
+        if tail_bars:
+            for t in range(max(0, n_tail - T), n_tail):
+                yield ("wait", f"q_tail{t % T}", t // T)
+                yield ("wait", f"do_tail{t % T}", t // T)
 
     def mma():
         gq = n_tail = 0
@@ -168,7 +172,7 @@ def _bwd_roles(items, fixed, head_dim=128, tail_bars=True):
             def q_in(i):
                 g = gq + i
                 if ragged and i == n_q - 1:
-                    yield ("wait", "tail_fixed", n_tail)
+                    yield ("wait", f"tail_fixed{n_tail % T}", n_tail // T)
                 else:
                     yield ("wait", f"q_full{g & 1}", g >> 1)
 
@@ -252,13 +256,13 @@ def _bwd_roles(items, fixed, head_dim=128, tail_bars=True):
                 yield ("arrive", f"q_ready{s}")
                 if ragged and i == n_q - 1:
                     if tail_bars:
-                        yield ("wait", "q_tail", n_tail)
-                        yield ("wait", "do_tail", n_tail)
+                        yield ("wait", f"q_tail{n_tail % T}", n_tail // T)
+                        yield ("wait", f"do_tail{n_tail % T}", n_tail // T)
                     else:
                         yield ("wait", f"q_full{s}", g >> 1)
                         yield ("wait", "do_full", g)
                     yield ("write", [f"Q{s}", "DO"])        # rows past the sample's end
-                    yield ("arrive", "tail_fixed")
+                    yield ("arrive", f"tail_fixed{n_tail % T}")
                     n_tail += 1
             gq += n_q
 
@@ -320,16 +324,17 @@ def _bwd_roles(items, fixed, head_dim=128, tail_bars=True):
     return roles
 
 
-def _bwd_barriers(head_dim=128):
+def _bwd_barriers(head_dim=128, tail_slots=2):
     nf = 2 if head_dim == 128 else 1
     readers = 5 if head_dim == 128 else 4        # MMA, row warp, two compute warpgroups (+ reducer)
     counts = {"kv_full": 1, "kv_ready": 2, "kv_empty": 1, "acc_full": 1, "fin": 1,
               "item_full0": 1, "item_full1": 1, "item_empty0": readers, "item_empty1": readers,
               "q_full0": 1, "q_full1": 1, "q_ready0": 1, "q_ready1": 1,
-              "q_free0": nf, "q_free1": nf, "do_full": 1, "do_free": 1, "q_tail": 1, "do_tail": 1,
-              "tail_fixed": 1, "s_full": 1, "p_ready": 2,
+              "q_free0": nf, "q_free1": nf, "do_full": 1, "do_free": 1, "s_full": 1, "p_ready": 2,
               "dp_full": 1, "ds_ready": 2, "a_free": 1, "dq_full": 1, "dq_free": 2, "stage_full0": 1,
               "stage_full1": 1, "stage_free": 1, "q_issued": 1}
+    for t in range(tail_slots):
+        counts.update({f"q_tail{t}": 1, f"do_tail{t}": 1, f"tail_fixed{t}": 1})
     return {n: Barrier(n, c) for n, c in counts.items()}
 
 
@@ -342,7 +347,7 @@ def _bwd_barriers(head_dim=128):
 # prep warps then zero them before PV reads the tile).
 # --------------------------------------------------------------------------
 
-def _fwd_roles(items, rng, k_stages=3, v_stages=2, pv_drain=True, item_ring=True, v_tail=True):
+def _fwd_roles(items, rng, k_stages=3, v_stages=2, pv_drain=True, item_ring=True, v_tail=True, tail_slots=2):
     """The item ring, the Q prologue, the K ring (k_stages), the V ring
     (v_stages), the ping-pong MMA order QK_0(j), PV_1(j-1), QK_1(j), PV_0(j),
     and the two softmax warpgroups, whose O rescale waits for the tile's
@@ -351,8 +356,11 @@ def _fwd_roles(items, rng, k_stages=3, v_stages=2, pv_drain=True, item_ring=True
     QK_a overwrites S_a; item_ring=False drops the producer's wait for the
     readers of an item slot; v_tail=False has the prep warps wait for a
     ragged item's last V tile on its slot's v_full, skipping that slot's
-    earlier phases (checks of the checker)."""
+    earlier phases; ragged item n uses v_tail / v_fixed n % tail_slots, and
+    tail_slots=1 shares one of each among all ragged items (checks of the
+    checker)."""
     n_items = len(items)
+    T = tail_slots
 
     def take(k):
         yield ("wait", f"item_full{k & 1}", k >> 1)
@@ -389,7 +397,7 @@ def _fwd_roles(items, rng, k_stages=3, v_stages=2, pv_drain=True, item_ring=True
                     yield ("wait", f"v_free{s}", g // v_stages - 1)
                 if items[k][1] and j == n - 1 and v_tail:
                     yield ("arrive", f"v_full{s}")          # the slot's phase, without the data
-                    yield ("tma", "v_tail", [f"V{s}"])
+                    yield ("tma", f"v_tail{n_tail % T}", [f"V{s}"])
                 else:
                     yield ("tma", f"v_full{s}", [f"V{s}"])
 
@@ -411,8 +419,9 @@ def _fwd_roles(items, rng, k_stages=3, v_stages=2, pv_drain=True, item_ring=True
                 yield ("wait", f"k_full{g % k_stages}", g // k_stages)
             for g in range(max(0, vc - v_stages), vc):
                 yield ("wait", f"v_full{g % v_stages}", g // v_stages)
-        if n_tail and v_tail:
-            yield ("wait", "v_tail", n_tail - 1)
+        if v_tail:
+            for t in range(max(0, n_tail - T), n_tail):
+                yield ("wait", f"v_tail{t % T}", t // T)
 
     def qk(a, g):
         return ("mma", [f"Q{a}", f"K{g % k_stages}"], [f"S{a}"], f"S{a}")
@@ -455,7 +464,7 @@ def _fwd_roles(items, rng, k_stages=3, v_stages=2, pv_drain=True, item_ring=True
                     yield ("commit", "q_empty1")
                 yield ("wait", "p_full0", g)
                 if ragged and j == n - 1:
-                    yield ("wait", "v_fixed", n_ragged)
+                    yield ("wait", f"v_fixed{n_ragged % T}", n_ragged // T)
                 else:
                     yield ("wait", f"v_full{g % v_stages}", g // v_stages)
                 yield pv(0, g)
@@ -487,11 +496,11 @@ def _fwd_roles(items, rng, k_stages=3, v_stages=2, pv_drain=True, item_ring=True
             if ragged:
                 g = vc + n - 1
                 if v_tail:
-                    yield ("wait", "v_tail", n_ragged)
+                    yield ("wait", f"v_tail{n_ragged % T}", n_ragged // T)
                 else:
                     yield ("wait", f"v_full{g % v_stages}", g // v_stages)
                 yield ("write", [f"V{g % v_stages}"])       # rows past the sample's end
-                yield ("arrive", "v_fixed")
+                yield ("arrive", f"v_fixed{n_ragged % T}")
                 n_ragged += 1
             vc += n
 
@@ -526,11 +535,12 @@ def _fwd_roles(items, rng, k_stages=3, v_stages=2, pv_drain=True, item_ring=True
     return {"producer": producer(), "mma": mma(), "prep": prep(), "sm0": softmax(0), "sm1": softmax(1)}
 
 
-def _fwd_barriers(k_stages=3, v_stages=2):
-    names = ["final", "s_full0", "s_full1", "p_full0", "p_full1", "pv_done0", "pv_done1", "v_tail", "v_fixed",
+def _fwd_barriers(k_stages=3, v_stages=2, tail_slots=2):
+    names = ["final", "s_full0", "s_full1", "p_full0", "p_full1", "pv_done0", "pv_done1",
              "item_full0", "item_full1", "q_full0", "q_full1", "q_ready0", "q_ready1", "q_empty0", "q_empty1"]
     names += [f"k_full{s}" for s in range(k_stages)] + [f"k_free{s}" for s in range(k_stages)]
     names += [f"v_full{s}" for s in range(v_stages)] + [f"v_free{s}" for s in range(v_stages)]
+    names += [f"v_tail{t}" for t in range(tail_slots)] + [f"v_fixed{t}" for t in range(tail_slots)]
     bars = {n: Barrier(n, 1) for n in names}
     for s in range(2):
         bars[f"item_empty{s}"] = Barrier(f"item_empty{s}", 4)   # MMA, prep, two softmax warpgroups
@@ -542,7 +552,7 @@ def _fwd_barriers(k_stages=3, v_stages=2):
 # --------------------------------------------------------------------------
 
 def run_schedule(n, seed, fixed=True, kernel="bwd", head_dim=128, pv_drain=True, item_ring=True,
-                 v_tail=True, tail_bars=True, max_steps=400000):
+                 v_tail=True, tail_bars=True, tail_slots=2, max_steps=400000):
     """One random interleaving of `kernel`'s protocol over the work items
     n = [(Q tiles, ragged), ...] (backward) or [(K/V tiles, ragged), ...]
     (forward).  Returns None when every role finished, or a string
@@ -550,10 +560,11 @@ def run_schedule(n, seed, fixed=True, kernel="bwd", head_dim=128, pv_drain=True,
     data race."""
     rng = random.Random(seed)
     if kernel == "bwd":
-        bars, roles = _bwd_barriers(head_dim), _bwd_roles(n, fixed, head_dim, tail_bars)
+        bars, roles = _bwd_barriers(head_dim, tail_slots), _bwd_roles(n, fixed, head_dim, tail_bars, tail_slots)
     else:
-        bars, roles = _fwd_barriers(), _fwd_roles(n, random.Random(seed + 7919), pv_drain=pv_drain,
-                                                 item_ring=item_ring, v_tail=v_tail)
+        bars, roles = _fwd_barriers(tail_slots=tail_slots), _fwd_roles(n, random.Random(seed + 7919), pv_drain=pv_drain,
+                                                                       item_ring=item_ring, v_tail=v_tail,
+                                                                       tail_slots=tail_slots)
     nxt = {r: next(g) for r, g in roles.items()}
     vc = {r: {r: 1} for r in roles}
     weight = {r: rng.choice([0.02, 0.2, 1.0, 1.0, 5.0]) for r in roles}  # some roles run far behind
@@ -671,6 +682,7 @@ BWD_ITEM_LISTS = [
     [(1, True)], [(2, False)], [(3, True), (3, True)], [(5, False), (1, True), (2, True)],
     [(1, False), (1, True), (1, False), (2, True)], [(8, True), (4, False)],
     [(2, True), (3, False), (1, True), (4, True), (2, False)],
+    [(2, True), (1, True), (1, True)], [(1, True), (1, False), (1, True), (1, True), (1, True)],
 ]
 
 
@@ -685,6 +697,7 @@ FWD_ITEM_LISTS = [
     [(1, True)], [(2, False)], [(3, True), (3, True)], [(4, False), (1, True), (2, True)],
     [(1, False), (1, True), (1, False), (1, True)], [(5, True), (2, False), (7, True)],
     [(2, True), (3, False), (1, True), (4, True), (2, False)],
+    [(2, True), (1, True), (1, True)], [(1, True), (1, True), (1, True), (1, True), (1, True)],
 ]
 
 
@@ -757,6 +770,19 @@ def test_checker_finds_a_skipped_phase_wait_in_the_backward():
         except (Overrun, Race):
             return
     pytest.fail("the checker missed the skipped-phase wait")
+
+
+@pytest.mark.parametrize("kernel", ["fwd", "bwd"])
+def test_checker_finds_a_shared_tail_barrier(kernel):
+    """One set of tail barriers for every ragged item: two short ragged items
+    in a row can complete two phases of a tail barrier before its waiter
+    looked (the second tail needs only the other ring slot)."""
+    for seed in range(2000):
+        try:
+            run_schedule([(2, True), (1, True), (1, True)], seed, kernel=kernel, tail_slots=1)
+        except (Overrun, Race):
+            return
+    pytest.fail("the checker missed the shared tail barrier")
 
 
 def test_checker_finds_a_stale_drain_phase():
