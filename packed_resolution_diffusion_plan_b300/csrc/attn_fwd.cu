@@ -299,25 +299,31 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     } else if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(kTile, kTile, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(kTile, D, false, true);
-      const uint32_t sQ = smem_u32(smem + C::kOffQ);
-      const uint32_t sK = smem_u32(smem + C::kOffK);
-      const uint32_t sV = smem_u32(smem + C::kOffV);
+      // Descriptor low halves of the operand tiles (K-major Q and K: 16-byte
+      // leading and 1024-byte stride; MN-major V: two 64-element halves 16 KB
+      // apart), built once per MMA group from an opaque base and advanced
+      // per MMA by a constant add: the issuing thread's work per MMA is one
+      // add and the issue itself, since issuing is what bounds this thread.
+      const uint32_t s0 = smem_u32(smem);
+      constexpr uint32_t kHi = sdesc_hi<1024>();
+      auto klo = [&](int off) { return sdesc_lo<16>(opaque_u32(s0 + off)); };
+      auto mlo = [&](int off) { return sdesc_lo<16384>(opaque_u32(s0 + off)); };
       auto issue_qk = [&](int a, long long g) {
-        const uint32_t kb = sK + static_cast<uint32_t>(g % C::kKStages) * C::kTileBytes;
+        const uint32_t qa = klo(C::kOffQ + a * C::kTileBytes);
+        const uint32_t kb = klo(C::kOffK + static_cast<int>(g % C::kKStages) * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kColS + a * kTile, sdesc<16, 1024>(sQ + a * C::kTileBytes + off), sdesc<16, 1024>(kb + off),
-                 idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t off = static_cast<uint32_t>((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss_lh(tmem + C::kColS + a * kTile, qa + off, kb + off, kHi, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.s_full[a]);
       };
       auto issue_pv = [&](int a, long long g, bool first) {
-        const uint32_t vb = sV + static_cast<uint32_t>(g % C::kVStages) * C::kTileBytes;
+        const uint32_t vb = mlo(C::kOffV + static_cast<int>(g % C::kVStages) * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + C::kColO + a * D, tmem + C::kColS + a * kTile + kk * 8, sdesc<16384, 1024>(vb + kk * 2048),
-                 idesc_pv, (!first || kk > 0) ? 1u : 0u);
+          mma_ts_lh(tmem + C::kColO + a * D, tmem + C::kColS + a * kTile + kk * 8, vb + kk * 128, kHi, idesc_pv,
+                    (!first || kk > 0) ? 1u : 0u);
         mma_commit(&bars.pv_done[a]);
       };
       long long gs = 0;   // K/V steps of the previous items: the position of every per-step barrier
