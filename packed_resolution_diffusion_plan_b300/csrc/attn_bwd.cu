@@ -83,9 +83,9 @@ static_assert(2 * kRegsCompute + kRegsCtrl <= 3 * 168, "warpgroup register share
 // A timeout record names a barrier by its position here: kv_full 0, kv_ready
 // 1, kv_empty 2, acc_full 3, fin 4, item_full 5-6, item_empty 7-8, q_full
 // 9-10, q_ready 11-12, q_free 13-14, do_full 15, do_free 16, q_tail 17-18,
-// do_tail 19-20, tail_fixed 21-22, s_full 23, p_ready 24, dp_full 25,
-// ds_ready 26, a_free 27, dq_full 28, dq_free 29, stage_full 30-31,
-// stage_free 32, q_issued 33.
+// do_tail 19-20, tail_fixed 21-22, s_full 23, p_ready 24-25, dp_full 26,
+// ds_ready 27-28, a_free 29, dq_full 30, dq_free 31, stage_full 32-33,
+// stage_free 34, q_issued 35.
 // The last Q tile of an item whose sample ends inside it (a "ragged" item)
 // lands on q_tail / do_tail instead of its slots' q_full / do_full (whose
 // phases the producer completes with plain arrivals, so that they stay in
@@ -95,7 +95,7 @@ static_assert(2 * kRegsCompute + kRegsCtrl <= 3 * 168, "warpgroup register share
 // could complete two phases of a tail barrier before its waiter looked (the
 // next tail needs only the other q~ slot), and a parity wait would then
 // take the later phase for the one it wants.
-constexpr uint32_t kBwdBarriers = 34;
+constexpr uint32_t kBwdBarriers = 36;
 constexpr uint32_t kTimeoutKernelBwd = 2;
 // Arrivals on an item slot's "read" barrier: the MMA and reducer threads, the
 // row warp and the eight compute warps (one per warp).
@@ -105,7 +105,7 @@ struct BwdCtl {
   uint64_t item_full[2], item_empty[2];
   uint64_t q_full[2], q_ready[2], q_free[2], do_full, do_free;
   uint64_t q_tail[2], do_tail[2], tail_fixed[2];
-  uint64_t s_full, p_ready, dp_full, ds_ready, a_free, dq_full, dq_free;
+  uint64_t s_full, p_ready[2], dp_full, ds_ready[2], a_free, dq_full, dq_free;
   uint64_t stage_full[2], stage_free, q_issued;
   uint32_t tmem;
   int abort;
@@ -323,9 +323,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       mbar_init(&c.tail_fixed[s], 32);
     }
     mbar_init(&c.s_full, 1);
-    mbar_init(&c.p_ready, 2 * kTile);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&c.p_ready[s], kTile);   // compute warpgroup s: its P^T, then its dS^T
+      mbar_init(&c.ds_ready[s], kTile);
+    }
     mbar_init(&c.dp_full, 1);
-    mbar_init(&c.ds_ready, 2 * kTile);
     mbar_init(&c.a_free, 1);
     mbar_init(&c.dq_full, 1);
     mbar_init(&c.dq_free, 2 * kTile);
@@ -520,31 +522,38 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           const int s = static_cast<int>(g & 1), s1 = static_cast<int>((g + 1) & 1);
           const bool more = i + 1 < n_q;
           // dV += P^T_i dO_i, with P^T packed in the A columns each compute
-          // warpgroup read its S^T from (query 64c.. at column 64c).
-          if (!mbar_wait(&c.p_ready, g & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          {
-            const uint32_t b = mlo(C::kOffDO);
+          // warpgroup read its S^T from (query 64c.. at column 64c).  Both
+          // dV and dK reduce over the tile's queries, of which warpgroup c
+          // owns 64c..: each half is issued as soon as its warpgroup's
+          // operand is in place (the four MMAs of warpgroup 0's half run
+          // while warpgroup 1 still computes).
+          for (int cw = 0; cw < 2; ++cw) {
+            if (!mbar_wait(&c.p_ready[cw], g & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t b = mlo(C::kOffDO + cw * 64 * 128);
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ts_lh(tmem + C::kColDV, tmem + C::kColA + 64 * (kk >> 2) + 8 * (kk & 3), b + kk * 128, kHi,
-                        id_dv, (i > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts_lh(tmem + C::kColDV, tmem + C::kColA + 64 * cw + 8 * kk, b + kk * 128, kHi, id_dv,
+                        (i > 0 || cw > 0 || kk > 0) ? 1u : 0u);
           }
+          if (!ok) break;
           mma_commit(&c.do_free);
           // dk~ += dS^T_i q~_i, with dS^T packed in the A columns beside P^T
           // (query 64c.. at column 64c + 32).
-          if (!mbar_wait(&c.ds_ready, g & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          {
-            const uint32_t b = mlo(C::kOffQ + s * C::kTileBytes);
+          for (int cw = 0; cw < 2; ++cw) {
+            if (!mbar_wait(&c.ds_ready[cw], g & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t b = mlo(C::kOffQ + s * C::kTileBytes + cw * 64 * 128);
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ts_lh(tmem + C::kColDK, tmem + C::kColA + 32 + 64 * (kk >> 2) + 8 * (kk & 3), b + kk * 128, kHi,
-                        id_dk, (i > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts_lh(tmem + C::kColDK, tmem + C::kColA + 32 + 64 * cw + 8 * kk, b + kk * 128, kHi, id_dk,
+                        (i > 0 || cw > 0 || kk > 0) ? 1u : 0u);
           }
+          if (!ok) break;
           mma_commit(&c.a_free);  // dV_i and dK_i have read P^T and dS^T out of A
           mma_commit(&c.q_free[s]);
-          // dQ_i into B (the compute warps have read dP^T_i before ds_ready).
+          // dQ_i into B (each compute warpgroup has read its dP^T_i before
+          // its ds_ready).
           {
             const uint32_t bk = mlo(C::kOffK), bds = mlo(C::kOffDS);
 #pragma unroll
@@ -817,7 +826,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&c.p_ready);
+        mbar_arrive(&c.p_ready[cw]);
         if (!warp_wait(&c.dp_full, g & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -860,7 +869,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&c.ds_ready);
+        mbar_arrive(&c.ds_ready[cw]);
         if (i > 0 && cw == 0 && !dq_stage(g - 1, kTile)) { ok = false; break; }
       }
       if (ok) ok = dq_load(gq + n_q - 1, n_q - 1) && dq_stage(gq + n_q - 1, w.len - (n_q - 1) * kTile);

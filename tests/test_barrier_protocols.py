@@ -194,11 +194,15 @@ def _bwd_roles(items, fixed, head_dim=128, tail_bars=True, tail_slots=2):
             for i in range(n_q):
                 g = gq + i
                 s, s1 = g & 1, (g + 1) & 1
-                yield ("wait", "p_ready", g)
-                yield ("mma", ["A0P", "A1P", "DO"], ["DV"], "DV")    # dV += P^T dO
+                # dV += P^T dO and dK += dS^T q~ reduce over the queries: the
+                # half of compute warpgroup cw goes as soon as its operand is in
+                for cw in range(2):
+                    yield ("wait", f"p_ready{cw}", g)
+                    yield ("mma", [f"A{cw}P", "DO"], ["DV"], "DV")
                 yield ("commit", "do_free")
-                yield ("wait", "ds_ready", g)
-                yield ("mma", ["A0S", "A1S", f"Q{s}"], ["DK"], "DK")  # dK += dS^T q~
+                for cw in range(2):
+                    yield ("wait", f"ds_ready{cw}", g)
+                    yield ("mma", [f"A{cw}S", f"Q{s}"], ["DK"], "DK")
                 yield ("commit", "a_free")
                 yield ("commit", f"q_free{s}")
                 yield ("mma", ["K0", "K1", "DS0", "DS1"], ["B0", "B1"], "B")  # dQ_i
@@ -304,11 +308,11 @@ def _bwd_roles(items, fixed, head_dim=128, tail_bars=True, tail_slots=2):
                     yield ("wait", "s_full", g)
                     yield ("read", [f"A{cw}P", f"A{cw}S", f"ROW{s}"])   # S^T and -LSE2
                     yield ("write", [f"A{cw}P"])                       # P^T
-                    yield ("arrive", "p_ready")
+                    yield ("arrive", f"p_ready{cw}")
                     yield ("wait", "dp_full", g)
                     yield ("read", [f"B{cw}", f"ROW{s}"])              # dP^T and -D
                     yield ("write", [f"A{cw}S", f"DS{cw}"])            # dS^T
-                    yield ("arrive", "ds_ready")
+                    yield ("arrive", f"ds_ready{cw}")
                     if i > 0 and cw == 0:
                         yield from dq_stage(g - 1)
                 yield from dq_load(gq + n_q - 1)
@@ -330,8 +334,8 @@ def _bwd_barriers(head_dim=128, tail_slots=2):
     counts = {"kv_full": 1, "kv_ready": 2, "kv_empty": 1, "acc_full": 1, "fin": 1,
               "item_full0": 1, "item_full1": 1, "item_empty0": readers, "item_empty1": readers,
               "q_full0": 1, "q_full1": 1, "q_ready0": 1, "q_ready1": 1,
-              "q_free0": nf, "q_free1": nf, "do_full": 1, "do_free": 1, "s_full": 1, "p_ready": 2,
-              "dp_full": 1, "ds_ready": 2, "a_free": 1, "dq_full": 1, "dq_free": 2, "stage_full0": 1,
+              "q_free0": nf, "q_free1": nf, "do_full": 1, "do_free": 1, "s_full": 1, "p_ready0": 1, "p_ready1": 1,
+              "dp_full": 1, "ds_ready0": 1, "ds_ready1": 1, "a_free": 1, "dq_full": 1, "dq_free": 2, "stage_full0": 1,
               "stage_full1": 1, "stage_free": 1, "q_issued": 1}
     for t in range(tail_slots):
         counts.update({f"q_tail{t}": 1, f"do_tail{t}": 1, f"tail_fixed{t}": 1})
