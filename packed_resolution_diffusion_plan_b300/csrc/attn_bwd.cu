@@ -97,9 +97,13 @@ static_assert(2 * kRegsCompute + kRegsCtrl <= 3 * 168, "warpgroup register share
 // take the later phase for the one it wants.
 constexpr uint32_t kBwdBarriers = 36;
 constexpr uint32_t kTimeoutKernelBwd = 2;
-// Arrivals on an item slot's "read" barrier: the MMA and reducer threads, the
-// row warp and the eight compute warps (one per warp).
-constexpr uint32_t kItemReaders = 1 + 1 + 1 + 8;
+// Arrivals on an item slot's "read" barrier: the MMA thread, the reducer
+// thread (head_dim 128 only: with 64, dQ leaves by atomics and the reducer
+// warp has no role), the row warp and the eight compute warps (one per warp).
+template <int D>
+constexpr uint32_t item_readers() {
+  return 1 + (D == 128 ? 1 : 0) + 1 + 8;
+}
 struct BwdCtl {
   uint64_t kv_full, kv_ready, kv_empty, acc_full, fin;
   uint64_t item_full[2], item_empty[2];
@@ -306,7 +310,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     mbar_init(&c.fin, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&c.item_full[s], 1);
-      mbar_init(&c.item_empty[s], kItemReaders);
+      mbar_init(&c.item_empty[s], item_readers<D>());
       mbar_init(&c.q_full[s], 1);
       mbar_init(&c.q_ready[s], 32);  // the row warp's lanes
       // head_dim 128: dK_i has read the slot, and the reducer has read the

@@ -65,6 +65,16 @@ def test_bwd_text_only_and_image_only_samples(head_dim):
               heads=2, head_dim=head_dim, seed=head_dim)
 
 
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_bwd_runs_of_short_ragged_samples(head_dim):
+    # 200 samples of at most 124 tokens, 8 heads: every work item is one
+    # K/V tile whose only Q tile is ragged, about 11 in a row per CTA, so
+    # the two sets of ragged-tail barriers take turns many times
+    samples = synth.random_pack(950 + head_dim, 200, 60, 8)
+    assert max(t + (h // 16) * (w // 16) for t, h, w in samples) < 128
+    _run_full(samples, heads=8, head_dim=head_dim, seed=head_dim)
+
+
 def test_bwd_single_token_closed_form():
     """One key: P = 1, dS = 0, so dQ = dK = 0 and dV = dO."""
     plan, (q, k, v, do), (dq, dk, dv) = _gpu_fwd_bwd([(0, 16, 16), (1, 16, 16)], 2, 128, 3)

@@ -57,6 +57,16 @@ def test_fwd_text_only_and_image_only_samples(head_dim):
               heads=2, head_dim=head_dim, seed=head_dim)
 
 
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_fwd_runs_of_short_ragged_samples(head_dim):
+    # 200 samples of at most 124 tokens, 8 heads: every work item is one
+    # ragged K/V tile, about 11 in a row per CTA, so the two sets of
+    # ragged-tail barriers take turns many times within one launch
+    samples = synth.random_pack(900 + head_dim, 200, 60, 8)
+    assert max(t + (h // 16) * (w // 16) for t, h, w in samples) < 128
+    _run_full(samples, heads=8, head_dim=head_dim, seed=head_dim)
+
+
 def test_fwd_custom_scale_and_budget():
     samples = [(30, 96, 96), (12, 64, 48), (0, 48, 160)]
     _run_full(samples, heads=2, head_dim=64, seed=4, scale=0.3)
