@@ -328,8 +328,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     }
     mbar_init(&c.s_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&c.p_ready[s], kTile);   // compute warpgroup s: its P^T, then its dS^T
-      mbar_init(&c.ds_ready[s], kTile);
+      mbar_init(&c.p_ready[s], kTile);    // compute warpgroup s's P^T is in TMEM
+      mbar_init(&c.ds_ready[s], kTile);   // its dS^T is in TMEM and shared memory
     }
     mbar_init(&c.dp_full, 1);
     mbar_init(&c.a_free, 1);
