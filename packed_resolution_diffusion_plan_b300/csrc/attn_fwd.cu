@@ -214,8 +214,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
       const bool drop = (args.g.debug & kDebugDropFwdKV) != 0;  // timeout-path tests only
-      long long kc = 0, vc = 0;            // K / V tiles of the previous items (the rings' positions)
-      long long k_issued = 0, v_issued = 0;  // K / V loads issued so far
+      // Per-CTA step counters are 32-bit (a CTA runs far fewer than 2^31 K/V
+      // steps): the issuing thread derives ring slots and phases from them
+      // every step, and a 64-bit division by the stage count is a long
+      // multi-instruction sequence.
+      int kc = 0, vc = 0;            // K / V tiles of the previous items (the rings' positions)
+      int k_issued = 0, v_issued = 0;  // K / V loads issued so far
       int q_issued = 0;                    // Q tile loads issued so far
       int tail_issued = 0;                 // loads issued on v_tail
       bool ok = true;
@@ -244,7 +248,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           return true;
         };
         auto load_k = [&](int j) -> bool {
-          const long long g = kc + j;
+          const int g = kc + j;
           const int s = static_cast<int>(g % C::kKStages);
           if (g >= C::kKStages && !mbar_wait(&bars.k_free[s], (g / C::kKStages - 1) & 1, abort_flag)) return false;
           if (drop) return true;
@@ -256,7 +260,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           return true;
         };
         auto load_v = [&](int j) -> bool {
-          const long long g = vc + j;
+          const int g = vc + j;
           const int s = static_cast<int>(g % C::kVStages);
           if (g >= C::kVStages && !mbar_wait(&bars.v_free[s], (g / C::kVStages - 1) & 1, abort_flag)) return false;
           if (drop) return true;
@@ -290,9 +294,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       // Let this CTA's own copies land before its shared memory is released
       // (q_issued counts Q tile loads: item k's tile a is load 2k + a).
       for (int i = q_issued > 2 ? q_issued - 2 : 0; i < q_issued; ++i) wait_drain(&bars.q_full[i & 1], (i >> 1) & 1, abort_flag);
-      for (long long g = k_issued > C::kKStages ? k_issued - C::kKStages : 0; g < k_issued; ++g)
+      for (int g = k_issued > C::kKStages ? k_issued - C::kKStages : 0; g < k_issued; ++g)
         wait_drain(&bars.k_full[g % C::kKStages], (g / C::kKStages) & 1, abort_flag);
-      for (long long g = v_issued > C::kVStages ? v_issued - C::kVStages : 0; g < v_issued; ++g)
+      for (int g = v_issued > C::kVStages ? v_issued - C::kVStages : 0; g < v_issued; ++g)
         wait_drain(&bars.v_full[g % C::kVStages], (g / C::kVStages) & 1, abort_flag);
       for (int t = tail_issued > 2 ? tail_issued - 2 : 0; t < tail_issued; ++t)
         wait_drain(&bars.v_tail[t & 1], (t >> 1) & 1, abort_flag);
@@ -308,7 +312,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       constexpr uint32_t kHi = sdesc_hi<1024>();
       auto klo = [&](int off) { return sdesc_lo<16>(opaque_u32(s0 + off)); };
       auto mlo = [&](int off) { return sdesc_lo<16384>(opaque_u32(s0 + off)); };
-      auto issue_qk = [&](int a, long long g) {
+      auto issue_qk = [&](int a, int g) {
         const uint32_t qa = klo(C::kOffQ + a * C::kTileBytes);
         const uint32_t kb = klo(C::kOffK + static_cast<int>(g % C::kKStages) * C::kTileBytes);
 #pragma unroll
@@ -318,7 +322,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         mma_commit(&bars.s_full[a]);
       };
-      auto issue_pv = [&](int a, long long g, bool first) {
+      auto issue_pv = [&](int a, int g, bool first) {
         const uint32_t vb = mlo(C::kOffV + static_cast<int>(g % C::kVStages) * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
@@ -326,7 +330,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     (!first || kk > 0) ? 1u : 0u);
         mma_commit(&bars.pv_done[a]);
       };
-      long long gs = 0;   // K/V steps of the previous items: the position of every per-step barrier
+      int gs = 0;   // K/V steps of the previous items: the position of every per-step barrier
       int n_ragged = 0;   // items whose last V tile had rows past the sample's end
       bool ok = true;
       for (int k = 0; ok; ++k) {
@@ -340,7 +344,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // read it, so QK_a waits for the tile's previous PV_a (across items
         // too: the previous item's last PV_a).
         auto v_ready = [&](int j) -> bool {
-          const long long g = gs + j;
+          const int g = gs + j;
           if (ragged && j == n_kv - 1) return mbar_wait(&bars.v_fixed[n_ragged & 1], (n_ragged >> 1) & 1, abort_flag);
           return mbar_wait(&bars.v_full[g % C::kVStages], (g / C::kVStages) & 1, abort_flag);
         };
@@ -352,7 +356,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         issue_qk(0, gs);
         if (n_kv == 1) mma_commit(&bars.q_empty[0]);
         for (int j = 0; ok && j < n_kv; ++j) {
-          const long long g = gs + j;
+          const int g = gs + j;
           if (j > 0) {
             if (!mbar_wait(&bars.p_full[1], (g - 1) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
@@ -403,7 +407,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     } else if (warp >= kPrepWarp0) {
       // The V tail of every ragged item (64 threads).
       const int t = tid - kPrepWarp0 * 32;
-      long long vc = 0;
+      int vc = 0;
       int n_ragged = 0;
       for (int k = 0;; ++k) {
         WorkItem w;
@@ -413,7 +417,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         if (last_valid < kTile) {
           // Zero the last V tile's rows past the sample's end (their P is 0,
           // but 0 times a non-finite value is not).
-          const long long g = vc + n_kv - 1;
+          const int g = vc + n_kv - 1;
           if (!warp_wait(&bars.v_tail[n_ragged & 1], (n_ragged >> 1) & 1, abort_flag)) break;
           uint8_t* vt = smem + C::kOffV + static_cast<int>(g % C::kVStages) * C::kTileBytes;
           for (int c = t; c < (kTile - last_valid) * 8 * C::kHalves; c += kPrepThreads) {
@@ -456,7 +460,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       mbar_arrive(&bars.q_ready[a]);
       return true;
     };
-    long long gs = 0;
+    int gs = 0;
     WorkItem w;
     bool ok = prologue(0, &w);
     for (int k = 0; ok && w.sample >= 0; ++k) {
@@ -466,7 +470,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       const int last_valid = w.len - (n_kv - 1) * kTile;
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n_kv; ++j) {
-        const long long g = gs + j;
+        const int g = gs + j;
         if (!warp_wait(&bars.s_full[a], g & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[4][32];
